@@ -1,0 +1,252 @@
+/*
+ * prune24.h -- C ABI of libprune24: 2:4 semi-structured sparse training of
+ * transformer FFN layers on one NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute (sources: web pages on N:M sparse training, cited by
+ * title and section):
+ *   - inno4scale "Success story ESPLAG", "Research Topic" / "Solution":
+ *     N:M (here 2:4) semi-structured magnitude pruning, a compressed storage
+ *     format, a sparse matrix-matrix multiply (SpMM) on sparse tensor cores,
+ *     gradual magnitude pruning, and a sparse version of the whole training step.
+ *   - NSF PAR award 2340011 listing, SLOPE abstract: the double-pruned backward
+ *     pass -- the transposed, already-pruned weight is pruned again with N:M so
+ *     that the backward GEMM is sparse as well.
+ *   - "To 2:4 Sparsity and Beyond: Neuron-level Activation Function to
+ *     Accelerate LLM Pre-Training", abstract: 2:4 weights in every FFN matmul,
+ *     with sparse activations on top.
+ *   - "Sparser, Faster, Lighter Transformer Language Models", training
+ *     strategy: ReLU as the FFN activation.
+ *
+ * Conventions (all calls):
+ *   - Matrices are row-major. bf16 = 16-bit brain float, passed as void*.
+ *     Every pointer marked "device" is CUDA device memory on the current device.
+ *   - The caller owns all memory. The library never allocates or frees device
+ *     memory and never synchronises, except p24_query_status.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and returns a p24_status. Arguments are validated on the
+ *     host before anything is launched; on an error nothing is launched.
+ *   - Alignment: every device base pointer must be 16-byte aligned and every
+ *     row stride must be a multiple of 16 bytes (P24_EALIGN otherwise).
+ *   - 2:4 rule: in each group of 4 consecutive elements along the pruned axis,
+ *     the two of largest magnitude are kept; magnitude is the bf16 bit pattern
+ *     with the sign cleared, compared as an unsigned integer (so -0 == +0 and
+ *     NaN sorts above inf); equal magnitudes go to the lower index.
+ *   - The library is stateless apart from one device status word per GPU,
+ *     written by kernels whose bounded waits expired (see p24_query_status).
+ */
+#ifndef PRUNE24_H
+#define PRUNE24_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  P24_OK = 0,
+  P24_EINVAL = -1,        /* null pointer, bad shape, bad flag */
+  P24_EALIGN = -2,        /* pointer or row stride not 16-byte aligned */
+  P24_ECUDA = -3,         /* a CUDA runtime/driver call or launch failed */
+  P24_ETIMEOUT = -4,      /* a kernel's bounded wait expired (device status word) */
+  P24_EUNSUPPORTED = -5,  /* no sm_103a device, or a shape outside the supported set */
+  P24_ENOSPACE = -6       /* workspace smaller than required */
+} p24_status;
+
+/*
+ * A matrix pruned 2:4 along its columns, in compressed form (the "tailored
+ * compressed storage format" of the ESPLAG success story, "Solution"; the
+ * 2:4 case of values + 2-bit indices).
+ *   rows, cols : logical dense shape; cols % 4 == 0.
+ *   vals       : device bf16 [rows, ldv]. Group g of row r keeps two values,
+ *                stored at vals[r*ldv + 2g] and [2g+1] in ascending index order.
+ *                Entries from cols/2 to ldv-1 are zero padding.
+ *   meta       : device uint8 [rows, ldm]. Group g's nibble i0 | (i1 << 2)
+ *                (0 <= i0 < i1 <= 3 are the kept positions) sits in byte g/2,
+ *                low nibble for even g. Unused nibbles up to ldm are 0x4.
+ *   ldv        : >= p24_ld_vals(cols), multiple of 8 (16 bytes).
+ *   ldm        : >= p24_ld_meta(cols), multiple of 16. The sparse GEMMs read
+ *                16 metadata bytes per 128 columns, so this rounding is needed.
+ */
+typedef struct {
+  void* vals;
+  uint8_t* meta;
+  int64_t rows;
+  int64_t cols;
+  int64_t ldv;
+  int64_t ldm;
+} p24_sparse;
+
+/* Smallest legal strides of a compressed row of `cols` columns. */
+int64_t p24_ld_vals(int64_t cols); /* round_up(cols/2, 8) elements */
+int64_t p24_ld_meta(int64_t cols); /* 16 * ceil(cols/128) bytes */
+
+/*
+ * prune24_compress -- 2:4 magnitude pruning along the columns of W and
+ * compression into values + metadata (ESPLAG success story, "Solution";
+ * "To 2:4 Sparsity and Beyond", abstract: 2:4 for the weights).
+ *   W       : device bf16 [rows, ldw], read only. cols % 4 == 0, ldw % 8 == 0.
+ *   out     : descriptor of the output (vals/meta device buffers owned by the
+ *             caller); out->rows == rows, out->cols == cols. All of vals and
+ *             meta up to the strides is written, padding included.
+ *   W_masked: optional device bf16 [rows, ldwm]: W with the pruned entries set
+ *             to +0 (the dense form of the pruned matrix). NULL to skip.
+ * Integer work only: the outputs are a pure function of the bits of W.
+ */
+int prune24_compress(const void* W, int64_t rows, int64_t cols, int64_t ldw,
+                     const p24_sparse* out, void* W_masked, int64_t ldwm,
+                     void* stream);
+
+/*
+ * prune24_transpose_repack -- the double prune of the SLOPE abstract: W_fwd
+ * (given compressed, [N, K], 2:4 along K) is transposed to [K, N] and pruned
+ * 2:4 again along N with the same rule, then compressed.
+ *   fwd  : input descriptor, rows = N (N % 4 == 0), cols = K.
+ *   bwdT : output descriptor, rows = K, cols = N. Written in full.
+ * A column group with fewer than two nonzeros keeps zeros at the lowest free
+ * indices, so the selected positions of bwdT need not lie inside the forward
+ * mask, while its nonzero entries always do.
+ */
+int prune24_transpose_repack(const p24_sparse* fwd, const p24_sparse* bwdT,
+                             void* stream);
+
+/*
+ * prune24_compress_both -- prune24_compress followed by
+ * prune24_transpose_repack in one pass over the dense W (the per-step mask
+ * recompute of gradual magnitude pruning, ESPLAG success story, "Research
+ * Topic"). rows % 4 == 0. Outputs are bit-identical to the two separate calls.
+ */
+int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw,
+                          const p24_sparse* fwd, const p24_sparse* bwdT,
+                          void* W_masked, int64_t ldwm, void* stream);
+
+/* Epilogue flags of the sparse GEMMs. */
+#define P24_EPI_BIAS  0x1u  /* add an fp32 bias per output column */
+#define P24_EPI_RELU  0x2u  /* ReLU after the bias (sets +0 for x <= 0) */
+#define P24_EPI_ACT24 0x4u  /* 2:4-prune the bf16 output along its columns */
+
+/*
+ * spmm24_fwd -- forward linear with a 2:4 weight on the sparse tensor cores
+ * (ESPLAG success story, "Research Topic": the SpMM):
+ *   Y = act(X . W^T + bias), accumulated in fp32, rounded once to bf16.
+ *   X     : device bf16 [M, ldx], K = W->cols columns.
+ *   W     : compressed weight, rows = N (output features), cols = K.
+ *   bias  : device fp32 [N] if flags has P24_EPI_BIAS, else ignored.
+ *   flags : P24_EPI_BIAS | P24_EPI_RELU | P24_EPI_ACT24.
+ *   Y     : device bf16 [M, ldy]. With P24_EPI_ACT24 it receives the pruned
+ *           output (zeros off the activation mask).
+ *   Y24   : with P24_EPI_ACT24, the compressed 2:4 form of Y along N
+ *           ("To 2:4 Sparsity and Beyond": sparse activations); rows = M,
+ *           cols = N (N % 4 == 0). NULL otherwise.
+ * The 2:4 decision is taken on the rounded bf16 values.
+ */
+int spmm24_fwd(const void* X, int64_t M, int64_t ldx, const p24_sparse* W,
+               const float* bias, uint32_t flags, void* Y, int64_t ldy,
+               const p24_sparse* Y24, void* stream);
+
+/*
+ * spmm24_fwd_sparse_act -- forward linear whose INPUT is the 2:4-sparse
+ * operand ("To 2:4 Sparsity and Beyond": sparse activations feeding the next
+ * FFN matmul):
+ *   Y = Xs . Wm^T + bias,   Xs compressed [M, K] (2:4 along K),
+ *   Wm : device bf16 [N, ldw] dense weight (normally the weight on its own
+ *        2:4 mask, as prune24_compress's W_masked writes it).
+ *   flags : P24_EPI_BIAS | P24_EPI_RELU.
+ */
+int spmm24_fwd_sparse_act(const p24_sparse* Xs, const void* Wm, int64_t N,
+                          int64_t ldw, const float* bias, uint32_t flags,
+                          void* Y, int64_t ldy, void* stream);
+
+/*
+ * spmm24_bwd_dx -- input gradient through a double-pruned weight (SLOPE
+ * abstract):  dX = (dY . W_bwd) * [gate > 0].
+ *   dY    : device bf16 [M, lddy], N = WbwdT->cols columns.
+ *   WbwdT : compressed W_bwd^T, rows = K, cols = N (2:4 along N), as
+ *           prune24_transpose_repack writes it.
+ *   gate  : optional device bf16 [M, ldg] (the forward ReLU output); where
+ *           gate <= 0 the gradient is 0 (ReLU'(0) = 0). NULL = no gate.
+ *   dX    : device bf16 [M, lddx], K columns.
+ */
+int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT,
+                  const void* gate, int64_t ldg, void* dX, int64_t lddx,
+                  void* stream);
+
+/*
+ * masked_dw_gemm -- weight gradient of a 2:4 linear, kept on the forward mask:
+ *   dW = (dY^T . X) * mask(Wfwd), a dense contraction over M in fp32.
+ *   dY   : device bf16 [M, lddy], N columns;  X : device bf16 [M, ldx], K columns.
+ *   Wfwd : the forward weight's descriptor; only its meta is read (N rows, K cols).
+ *   dW   : device bf16 [N, lddw]; entries off the mask are written as +0.
+ */
+int masked_dw_gemm(const void* dY, int64_t lddy, const void* X, int64_t ldx,
+                   int64_t M, const p24_sparse* Wfwd, void* dW, int64_t lddw,
+                   void* stream);
+
+/*
+ * p24_colsum -- bias gradient: out[n] = sum over m of G[m, n] (fp32 result,
+ * fp32 partial sums combined in a fixed order, so repeated calls are
+ * bit-identical).
+ *   G   : device bf16 [M, ldg], N columns;  out : device fp32 [N].
+ *   ws  : device scratch of at least p24_colsum_workspace_size(M, N) bytes.
+ */
+size_t p24_colsum_workspace_size(int64_t M, int64_t N);
+int p24_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* Flags of ffn24_step. */
+#define P24_STEP_ACT24 0x1u /* 2:4-prune ReLU(up) and feed it as the sparse operand of down */
+
+/*
+ * One FFN layer (up -> ReLU -> down), forward and backward, every matmul 2:4
+ * ("To 2:4 Sparsity and Beyond", abstract; ESPLAG "Research Topic"; SLOPE):
+ *   prune W_up, W_down 2:4 along their reduction axis and double-prune their
+ *   transposes (fresh masks every step);
+ *   H  = ReLU(X W_up^T + b_up)           (ACT24: H pruned 2:4 along ffn)
+ *   Y  = H W_down^T + b_down
+ *   dH = (dY W_down_bwd) * [H > 0];  db_up = colsum(dH);  db_down = colsum(dY)
+ *   dW_down = (dY^T H) on mask(W_down);  dX = dH W_up_bwd;  dW_up = (dH^T X) on mask(W_up)
+ * All tensors are dense, row-major, contiguous (row stride = column count):
+ *   X, dY, Y, dX : bf16 [M, d];  W_up, dW_up : bf16 [ffn, d];
+ *   W_down, dW_down : bf16 [d, ffn];  H : bf16 [M, ffn] (output, the stored
+ *   activation); b_up, db_up : fp32 [ffn];  b_down, db_down : fp32 [d].
+ *   b_up / b_down may be NULL (no bias); db_up / db_down may be NULL.
+ * d % 8 == 0 and ffn % 8 == 0.
+ */
+typedef struct {
+  int64_t M, d, ffn;
+  uint32_t flags;
+  const void* X;
+  const void* W_up;
+  const float* b_up;
+  const void* W_down;
+  const float* b_down;
+  const void* dY;
+  void* Y;
+  void* H;
+  void* dX;
+  void* dW_up;
+  void* dW_down;
+  float* db_up;
+  float* db_down;
+} p24_ffn_args;
+
+/* Device workspace ffn24_step needs for these sizes (compressed weights, dH, ...). */
+size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags);
+int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * p24_query_status -- synchronise `stream`, then return and clear the device
+ * status word of the current GPU: P24_OK, or P24_ETIMEOUT if a kernel gave up
+ * a bounded wait (the kernel then skipped its remaining work and exited
+ * cleanly, so the context stays usable).
+ */
+int p24_query_status(void* stream);
+
+/* Static text for a p24_status code. */
+const char* p24_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PRUNE24_H */

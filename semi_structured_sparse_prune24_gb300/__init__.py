@@ -1,0 +1,16 @@
+"""2:4 semi-structured sparse training of transformer FFN layers on NVIDIA GB300.
+
+The work is done by libprune24 (C ABI, include/prune24.h; CUDA kernels for
+sm_103a under csrc/). This package is its thin Python binding: the functions
+below carry the C names and only marshal torch tensors into pointers, sizes
+and strides. There is no CPU fallback.
+"""
+from ._native import (P24_EPI_ACT24, P24_EPI_BIAS, P24_EPI_RELU, P24_STEP_ACT24, P24Error, Sparse24,
+                      ffn24_step, ffn24_workspace_size, ld_meta, ld_vals, lib, masked_dw_gemm, p24_colsum,
+                      p24_query_status, prune24_compress, prune24_compress_both, prune24_transpose_repack,
+                      spmm24_bwd_dx, spmm24_fwd, spmm24_fwd_sparse_act)
+
+__all__ = ["P24Error", "Sparse24", "ffn24_step", "ffn24_workspace_size", "ld_meta", "ld_vals", "lib",
+           "masked_dw_gemm", "p24_colsum", "p24_query_status", "prune24_compress", "prune24_compress_both",
+           "prune24_transpose_repack", "spmm24_bwd_dx", "spmm24_fwd", "spmm24_fwd_sparse_act",
+           "P24_EPI_ACT24", "P24_EPI_BIAS", "P24_EPI_RELU", "P24_STEP_ACT24"]

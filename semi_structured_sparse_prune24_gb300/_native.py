@@ -1,0 +1,293 @@
+"""ctypes binding of libprune24 (include/prune24.h): argument marshalling only.
+
+Every call forwards raw device pointers, sizes and row strides of torch tensors
+to the C ABI and runs on the current torch CUDA stream; all arithmetic happens
+in the library's CUDA kernels. Output tensors the caller does not pass are
+allocated with torch (device memory is torch's job here). There is no CPU path:
+if the shared library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libprune24.so")
+
+P24_OK, P24_EINVAL, P24_EALIGN, P24_ECUDA, P24_ETIMEOUT, P24_EUNSUPPORTED, P24_ENOSPACE = 0, -1, -2, -3, -4, -5, -6
+P24_EPI_BIAS, P24_EPI_RELU, P24_EPI_ACT24 = 0x1, 0x2, 0x4
+P24_STEP_ACT24 = 0x1
+
+
+class P24Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {lib.p24_strerror(code).decode()} (status {code})")
+
+
+class p24_sparse(C.Structure):
+    _fields_ = [("vals", C.c_void_p), ("meta", C.c_void_p), ("rows", C.c_int64), ("cols", C.c_int64),
+                ("ldv", C.c_int64), ("ldm", C.c_int64)]
+
+
+class p24_ffn_args(C.Structure):
+    _fields_ = [("M", C.c_int64), ("d", C.c_int64), ("ffn", C.c_int64), ("flags", C.c_uint32),
+                ("X", C.c_void_p), ("W_up", C.c_void_p), ("b_up", C.c_void_p), ("W_down", C.c_void_p),
+                ("b_down", C.c_void_p), ("dY", C.c_void_p), ("Y", C.c_void_p), ("H", C.c_void_p),
+                ("dX", C.c_void_p), ("dW_up", C.c_void_p), ("dW_down", C.c_void_p), ("db_up", C.c_void_p),
+                ("db_down", C.c_void_p)]
+
+
+def _load() -> C.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libprune24 is not built ({_LIB_PATH} missing): run __graft_entry__.build() "
+                          "or python -m semi_structured_sparse_prune24_gb300.build")
+    L = C.CDLL(_LIB_PATH)
+    i64, vp, u32, sz, i32 = C.c_int64, C.c_void_p, C.c_uint32, C.c_size_t, C.c_int
+    sp = C.POINTER(p24_sparse)
+    sigs = {
+        "p24_ld_vals": (i64, [i64]),
+        "p24_ld_meta": (i64, [i64]),
+        "prune24_compress": (i32, [vp, i64, i64, i64, sp, vp, i64, vp]),
+        "prune24_transpose_repack": (i32, [sp, sp, vp]),
+        "prune24_compress_both": (i32, [vp, i64, i64, i64, sp, sp, vp, i64, vp]),
+        "spmm24_fwd": (i32, [vp, i64, i64, sp, vp, u32, vp, i64, sp, vp]),
+        "spmm24_fwd_sparse_act": (i32, [sp, vp, i64, i64, vp, u32, vp, i64, vp]),
+        "spmm24_bwd_dx": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, vp]),
+        "masked_dw_gemm": (i32, [vp, i64, vp, i64, i64, sp, vp, i64, vp]),
+        "p24_colsum_workspace_size": (sz, [i64, i64]),
+        "p24_colsum": (i32, [vp, i64, i64, i64, vp, vp, sz, vp]),
+        "ffn24_workspace_size": (sz, [i64, i64, i64, u32]),
+        "ffn24_step": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp]),
+        "p24_query_status": (i32, [vp]),
+        "p24_strerror": (C.c_char_p, [i32]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+def _check(code: int, where: str) -> None:
+    if code != P24_OK:
+        raise P24Error(code, where)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _mat(t: torch.Tensor, dtype=torch.bfloat16, name="tensor") -> tuple[int, int, int]:
+    """(rows, cols, row stride) of a row-major matrix view on a CUDA device."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libprune24 has no CPU path)")
+    if t.numel() and t.stride(1) != 1:
+        raise ValueError(f"{name} must be contiguous along its last dimension")
+    return t.shape[0], t.shape[1], (t.stride(0) if t.shape[0] > 1 else max(t.shape[1], t.stride(0)))
+
+
+def ld_vals(cols: int) -> int:
+    return int(lib.p24_ld_vals(cols))
+
+
+def ld_meta(cols: int) -> int:
+    return int(lib.p24_ld_meta(cols))
+
+
+@dataclass
+class Sparse24:
+    """A matrix pruned 2:4 along its columns, compressed (see p24_sparse in include/prune24.h).
+
+    vals: bf16 [rows, ldv] (torch tensor, may be a view with row stride ldv)
+    meta: uint8 [rows, ldm]
+    """
+    vals: torch.Tensor
+    meta: torch.Tensor
+    rows: int
+    cols: int
+
+    @staticmethod
+    def empty(rows: int, cols: int, device="cuda", ldv: int | None = None, ldm: int | None = None) -> "Sparse24":
+        ldv = ld_vals(cols) if ldv is None else ldv
+        ldm = ld_meta(cols) if ldm is None else ldm
+        vals = torch.empty((rows, ldv), dtype=torch.bfloat16, device=device)
+        meta = torch.empty((rows, ldm), dtype=torch.uint8, device=device)
+        return Sparse24(vals, meta, rows, cols)
+
+    @property
+    def ldv(self) -> int:
+        return self.vals.stride(0) if self.rows > 1 else self.vals.shape[1]
+
+    @property
+    def ldm(self) -> int:
+        return self.meta.stride(0) if self.rows > 1 else self.meta.shape[1]
+
+    def c(self) -> p24_sparse:
+        for t, name in ((self.vals, "vals"), (self.meta, "meta")):
+            if not t.is_cuda:
+                raise ValueError(f"Sparse24.{name} must be on a CUDA device")
+        return p24_sparse(self.vals.data_ptr(), self.meta.data_ptr(), self.rows, self.cols, self.ldv, self.ldm)
+
+
+# ------------------------------------------------------------------ entry points
+def prune24_compress(W: torch.Tensor, out: Sparse24 | None = None, W_masked: torch.Tensor | None = None,
+                     stream=None) -> Sparse24:
+    rows, cols, ldw = _mat(W, name="W")
+    out = Sparse24.empty(rows, cols, W.device) if out is None else out
+    ldwm = 0
+    if W_masked is not None:
+        _, _, ldwm = _mat(W_masked, name="W_masked")
+    d = out.c()
+    _check(lib.prune24_compress(W.data_ptr(), rows, cols, ldw, C.byref(d), _ptr(W_masked), ldwm, _stream(stream)),
+           "prune24_compress")
+    return out
+
+
+def prune24_transpose_repack(fwd: Sparse24, bwdT: Sparse24 | None = None, stream=None) -> Sparse24:
+    bwdT = Sparse24.empty(fwd.cols, fwd.rows, fwd.vals.device) if bwdT is None else bwdT
+    a, b = fwd.c(), bwdT.c()
+    _check(lib.prune24_transpose_repack(C.byref(a), C.byref(b), _stream(stream)), "prune24_transpose_repack")
+    return bwdT
+
+
+def prune24_compress_both(W: torch.Tensor, fwd: Sparse24 | None = None, bwdT: Sparse24 | None = None,
+                          W_masked: torch.Tensor | None = None, stream=None) -> tuple[Sparse24, Sparse24]:
+    rows, cols, ldw = _mat(W, name="W")
+    fwd = Sparse24.empty(rows, cols, W.device) if fwd is None else fwd
+    bwdT = Sparse24.empty(cols, rows, W.device) if bwdT is None else bwdT
+    ldwm = 0
+    if W_masked is not None:
+        _, _, ldwm = _mat(W_masked, name="W_masked")
+    a, b = fwd.c(), bwdT.c()
+    _check(lib.prune24_compress_both(W.data_ptr(), rows, cols, ldw, C.byref(a), C.byref(b), _ptr(W_masked), ldwm,
+                                     _stream(stream)), "prune24_compress_both")
+    return fwd, bwdT
+
+
+def spmm24_fwd(X: torch.Tensor, W: Sparse24, bias: torch.Tensor | None = None, relu: bool = False,
+               act24: bool = False, Y: torch.Tensor | None = None, Y24: Sparse24 | None = None, stream=None):
+    """Y = act(X W^T + bias); with act24 also returns the 2:4-compressed Y (Y, Y24)."""
+    M, K, ldx = _mat(X, name="X")
+    N = W.rows
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    _, _, ldy = _mat(Y, name="Y")
+    flags = (P24_EPI_BIAS if bias is not None else 0) | (P24_EPI_RELU if relu else 0)
+    y24c = None
+    if act24:
+        flags |= P24_EPI_ACT24
+        Y24 = Sparse24.empty(M, N, X.device) if Y24 is None else Y24
+        y24c = Y24.c()
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise TypeError("bias must be a CUDA float32 tensor")
+    w = W.c()
+    _check(lib.spmm24_fwd(X.data_ptr(), M, ldx, C.byref(w), _ptr(bias), flags, Y.data_ptr(), ldy,
+                          C.byref(y24c) if y24c is not None else None, _stream(stream)), "spmm24_fwd")
+    return (Y, Y24) if act24 else Y
+
+
+def spmm24_fwd_sparse_act(Xs: Sparse24, Wm: torch.Tensor, bias: torch.Tensor | None = None, relu: bool = False,
+                          Y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    N, K, ldw = _mat(Wm, name="Wm")
+    Y = torch.empty((Xs.rows, N), dtype=torch.bfloat16, device=Wm.device) if Y is None else Y
+    _, _, ldy = _mat(Y, name="Y")
+    flags = (P24_EPI_BIAS if bias is not None else 0) | (P24_EPI_RELU if relu else 0)
+    x = Xs.c()
+    _check(lib.spmm24_fwd_sparse_act(C.byref(x), Wm.data_ptr(), N, ldw, _ptr(bias), flags, Y.data_ptr(), ldy,
+                                     _stream(stream)), "spmm24_fwd_sparse_act")
+    return Y
+
+
+def spmm24_bwd_dx(dY: torch.Tensor, WbwdT: Sparse24, gate: torch.Tensor | None = None,
+                  dX: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    M, N, lddy = _mat(dY, name="dY")
+    K = WbwdT.rows
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device) if dX is None else dX
+    _, _, lddx = _mat(dX, name="dX")
+    ldg = 0
+    if gate is not None:
+        _, _, ldg = _mat(gate, name="gate")
+    w = WbwdT.c()
+    _check(lib.spmm24_bwd_dx(dY.data_ptr(), M, lddy, C.byref(w), _ptr(gate), ldg, dX.data_ptr(), lddx,
+                             _stream(stream)), "spmm24_bwd_dx")
+    return dX
+
+
+def masked_dw_gemm(dY: torch.Tensor, X: torch.Tensor, Wfwd: Sparse24, dW: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    M, N, lddy = _mat(dY, name="dY")
+    M2, K, ldx = _mat(X, name="X")
+    if M2 != M:
+        raise ValueError("dY and X must have the same number of rows")
+    dW = torch.empty((Wfwd.rows, Wfwd.cols), dtype=torch.bfloat16, device=dY.device) if dW is None else dW
+    _, _, lddw = _mat(dW, name="dW")
+    w = Wfwd.c()
+    _check(lib.masked_dw_gemm(dY.data_ptr(), lddy, X.data_ptr(), ldx, M, C.byref(w), dW.data_ptr(), lddw,
+                              _stream(stream)), "masked_dw_gemm")
+    return dW
+
+
+def p24_colsum(G: torch.Tensor, out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    M, N, ldg = _mat(G, name="G")
+    out = torch.empty(N, dtype=torch.float32, device=G.device) if out is None else out
+    need = int(lib.p24_colsum_workspace_size(M, N))
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=G.device)
+    _check(lib.p24_colsum(G.data_ptr(), M, N, ldg, out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+                          _stream(stream)), "p24_colsum")
+    return out
+
+
+def ffn24_workspace_size(M: int, d: int, ffn: int, act24: bool = False) -> int:
+    return int(lib.ffn24_workspace_size(M, d, ffn, P24_STEP_ACT24 if act24 else 0))
+
+
+def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict | None = None,
+               workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """One 2:4 FFN layer fwd+bwd; returns dict(Y, H, dX, dW_up, dW_down, db_up, db_down)."""
+    M, d, _ = _mat(X, name="X")
+    ffn = W_up.shape[0]
+    dev = X.device
+    for t, name, shape in ((W_up, "W_up", (ffn, d)), (W_down, "W_down", (d, ffn)), (dY, "dY", (M, d))):
+        _mat(t, name=name)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {shape} tensor")
+    o = {} if out is None else dict(out)
+    bf = torch.bfloat16
+    o.setdefault("Y", torch.empty((M, d), dtype=bf, device=dev))
+    o.setdefault("H", torch.empty((M, ffn), dtype=bf, device=dev))
+    o.setdefault("dX", torch.empty((M, d), dtype=bf, device=dev))
+    o.setdefault("dW_up", torch.empty((ffn, d), dtype=bf, device=dev))
+    o.setdefault("dW_down", torch.empty((d, ffn), dtype=bf, device=dev))
+    o.setdefault("db_up", torch.empty(ffn, dtype=torch.float32, device=dev))
+    o.setdefault("db_down", torch.empty(d, dtype=torch.float32, device=dev))
+    need = ffn24_workspace_size(M, d, ffn, act24)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    a = p24_ffn_args(M, d, ffn, P24_STEP_ACT24 if act24 else 0, X.data_ptr(), W_up.data_ptr(), _ptr(b_up),
+                     W_down.data_ptr(), _ptr(b_down), dY.data_ptr(), o["Y"].data_ptr(), o["H"].data_ptr(),
+                     o["dX"].data_ptr(), o["dW_up"].data_ptr(), o["dW_down"].data_ptr(), _ptr(o["db_up"]),
+                     _ptr(o["db_down"]))
+    _check(lib.ffn24_step(C.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "ffn24_step")
+    return o
+
+
+def p24_query_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return int(lib.p24_query_status(_stream(stream)))

@@ -1,0 +1,678 @@
+// gemm24_kernels.cu -- tensor-core GEMMs of the 2:4 FFN training step on
+// sm_103a: persistent, warp-specialised kernels with TMA-fed shared-memory
+// rings, tcgen05.mma accumulating in tensor memory (TMEM), and fused epilogues.
+//
+//  spmm_kernel      C[i, j] = sum_r A[i, r] B[j, r], A 2:4-sparse along r
+//                   (compressed values in smem, 2-bit metadata in TMEM,
+//                   tcgen05.mma.sp), B dense. Used for the forward linear
+//                   (A = weight, output written transposed), the double-pruned
+//                   backward dX (A = W_bwd^T, SLOPE abstract) and the linear
+//                   fed by 2:4 activations (A = activations, straight output).
+//  dw_kernel        dW[n, k] = sum_m dY[m, n] X[m, k] kept on the forward 2:4
+//                   mask: a dense contraction over tokens (both operands
+//                   MN-major), tcgen05.mma kind::f16.
+//
+// Sources: inno4scale "Success story ESPLAG" ("Research Topic": SpMM on sparse
+// tensor cores for the complete training step); SLOPE abstract (double-pruned
+// sparse backward); "To 2:4 Sparsity and Beyond" abstract (2:4 weights and
+// sparse activations in all FFN matmuls).
+//
+// Roles (warp index): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 epilogue
+// (warp w reads TMEM lanes 32*(w%4)..+31), 6-9 (spmm only) metadata movers:
+// smem -> registers -> TMEM, replacing rows past the matrix with a legal pattern.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "p24_internal.h"
+#include "p24_ptx.cuh"
+
+namespace p24 {
+namespace {
+
+constexpr int kBM = 128;  // MMA M: rows of A per tile = TMEM lanes
+
+// ---------------------------------------------------------------- params
+struct SpmmParams {
+  int rowsA, rowsB, K;  // K = logical (dense) reduction length
+  int tilesA, tilesB, num_tiles, group, nkb;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  const float* bias;
+  int relu;
+  const uint16_t* gate;
+  int64_t ldg;
+  uint16_t* a24_vals;
+  int64_t a24_ldv;
+  uint8_t* a24_meta;
+  int64_t a24_ldm;
+  int* status;
+};
+
+struct DwParams {
+  int N, K, M;  // dW is [N, K]; reduction over M
+  int tilesA, tilesB, num_tiles, group, nkb;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  const uint8_t* meta;
+  int64_t ldm;
+  int* status;
+};
+
+// Grouped raster: consecutive tiles walk `group` A-tiles before the next
+// B-tile, so a wave of CTAs shares a few A and B tiles through L2.
+__device__ __forceinline__ void tile_coords(int t, int tilesA, int tilesB, int group, int& ta, int& tb) {
+  const int per_group = group * tilesB;
+  const int g = t / per_group;
+  const int first = g * group;
+  const int gsize = min(group, tilesA - first);
+  const int r = t - g * per_group;
+  ta = first + r % gsize;
+  tb = r / gsize;
+}
+
+__device__ __forceinline__ uint32_t bf16_pos_mask(uint32_t w) {
+  // per 16-bit half: 0xFFFF where the bf16 value is > 0 (sign clear, not +0)
+  const uint32_t lo = ((w & 0x8000u) == 0 && (w & 0x7FFFu) != 0) ? 0x0000FFFFu : 0u;
+  const uint32_t hi = ((w & 0x80000000u) == 0 && (w & 0x7FFF0000u) != 0) ? 0xFFFF0000u : 0u;
+  return lo | hi;
+}
+
+// 2:4 pick on a group held as two words (see prune24_kernels.cu for the key).
+__device__ __forceinline__ uint32_t pick2_nibble(uint32_t lo, uint32_t hi) {
+  const uint32_t c0 = ((lo & 0x7FFFu) << 2) | 3u;
+  const uint32_t c1 = ((lo >> 14) & 0x1FFFCu) | 2u;
+  const uint32_t c2 = ((hi & 0x7FFFu) << 2) | 1u;
+  const uint32_t c3 = (hi >> 14) & 0x1FFFCu;
+  const uint32_t a = max(c0, c1), b = min(c0, c1);
+  const uint32_t c = max(c2, c3), d = min(c2, c3);
+  const uint32_t top = max(a, c);
+  const uint32_t second = max(min(a, c), max(b, d));
+  const uint32_t i_top = 3u - (top & 3u), i_sec = 3u - (second & 3u);
+  return min(i_top, i_sec) | (max(i_top, i_sec) << 2);
+}
+__device__ __forceinline__ uint32_t kept_pair(uint32_t lo, uint32_t hi, uint32_t nib) {
+  const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+  return __byte_perm(lo, hi, 0x1010u + i0 * 0x22u + i1 * 0x2200u);
+}
+__device__ __forceinline__ void mask_group(uint32_t& lo, uint32_t& hi, uint32_t nib) {
+  const uint32_t kb = (1u << (nib & 3u)) | (1u << (nib >> 2));
+  lo &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
+  hi &= ((kb & 4u) ? 0x0000FFFFu : 0u) | ((kb & 8u) ? 0xFFFF0000u : 0u);
+}
+
+__device__ __forceinline__ void tc_st_32x32b_x2(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- sparse GEMM
+// Per stage (64 logical K): A 128 rows x 32 compressed bf16 (64 B rows,
+// 64B swizzle), B BN rows x 64 bf16 (128 B rows, 128B swizzle), metadata
+// 128 rows x 16 B (the 8 bytes of this stage sit at (kb & 1) * 8).
+template <int BN, int STAGES>
+struct SpmmSmem {
+  static constexpr int kA = kBM * 64;   // bytes per stage
+  static constexpr int kB = BN * 128;
+  static constexpr int kE = kBM * 16;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + STAGES * kA;
+  static constexpr int kOffE = kOffB + STAGES * kB;
+  static constexpr int kOffStage = kOffE + STAGES * kE;  // epilogue transpose, 4 warps x 32x32 bf16
+  static constexpr int kOffBar = kOffStage + 4 * 32 * 32 * 2;
+  static constexpr int kBytes = kOffBar + 8 * (4 * STAGES + 4) + 16;
+  static constexpr int kTx = kA + kB + kE;
+};
+
+template <int BN, int STAGES, bool kTransOut>
+__global__ void __launch_bounds__(320, 1)
+    spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
+  using L = SpmmSmem<BN, STAGES>;
+  constexpr int kAccCols = 256;             // accumulator buffer b starts at column 256 * b
+  constexpr int kMetaCol0 = 256 + BN;       // then 2 metadata columns per stage
+  static_assert(BN <= 256 && 256 + BN + 2 * STAGES <= 512, "TMEM budget");
+  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, /*sparse=*/true, false, false);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* meta_ready = empty + STAGES;
+  uint64_t* acc_full = meta_ready + STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;         // [2]
+  uint64_t* spare = acc_empty + 2;            // [STAGES] unused
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + STAGES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&meta_ready[s], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(spare, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmE);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int ta, tb;
+        tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], L::kTx);
+          tma_load_2d(smem + L::kOffA + s * L::kA, &tmA, &full[s], kb * 32, ta * kBM);
+          tma_load_2d(smem + L::kOffB + s * L::kB, &tmB, &full[s], kb * 64, tb * BN);
+          tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &full[s], (kb >> 1) * 16, ta * kBM);
+        }
+      }
+      // Drain: every issued load must land before the CTA may exit.
+      const uint32_t n_drain = it < STAGES ? it : STAGES;
+      for (uint32_t i = 0; i < n_drain; ++i) {
+        const uint32_t j = it - 1 - i;
+        p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    uint32_t it = 0, tl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1;
+      if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + b * kAccCols;
+      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!p24_wait(&full[s], ph, abort_flag, p.status) ||
+            !p24_wait(&meta_ready[s], ph, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
+          const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint64_t adesc = smem_desc(a_base + j * 32, 16, 512, kSwizzle64B);
+            const uint64_t bdesc = smem_desc(b_base + j * 64, 16, 1024, kSwizzle128B);
+            tc_mma_sp_f16(d_tmem, adesc, bdesc, tmem + kMetaCol0 + 2 * s + j, kIdesc, (kb | j) != 0);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&acc_full[b]);
+      __syncwarp();
+    }
+    // Make sure no MMA is still running before TMEM is released.
+    if (lane == 0) {
+      tc_commit(spare);
+      p24_wait_quiet(spare, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------ metadata movers
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      int ta, tb;
+      tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      const bool row_ok = ta * kBM + row < p.rowsA;
+      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!p24_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
+        const uint2 e = *reinterpret_cast<const uint2*>(smem + L::kOffE + s * L::kE + row * 16 + (kb & 1) * 8);
+        const uint32_t e0 = row_ok ? e.x : 0x44444444u;
+        const uint32_t e1 = row_ok ? e.y : 0x44444444u;
+        tc_st_32x32b_x2(tmem + (static_cast<uint32_t>(q * 32) << 16) + kMetaCol0 + 2 * s, e0, e1);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta_ready[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2-5)
+    const int q = warp & 3;
+    uint16_t* stage = reinterpret_cast<uint16_t*>(smem + L::kOffStage) + q * 32 * 32;
+    uint32_t tl = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
+      int ta, tb;
+      tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      const int b = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1;
+      if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+      const int a_row = ta * kBM + q * 32 + lane;  // row of A held by this thread
+      if (kTransOut) {
+        // out[j, a_row]: token j (B row) x feature a_row (A row)
+        const float bias_v = (p.bias && a_row < p.rowsA) ? p.bias[a_row] : 0.f;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(acc + c * 32, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float f = __uint_as_float(v[j]) + bias_v;
+            if (p.relu) f = fmaxf(f, 0.f);
+            __nv_bfloat16 h = __float2bfloat16_rn(f);
+            stage[j * 32 + lane] = *reinterpret_cast<uint16_t*>(&h);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = r * 8 + (lane >> 2);
+            const int piece = lane & 3;
+            const int m = tb * BN + c * 32 + j;
+            const int n = ta * kBM + q * 32 + piece * 8;
+            uint4 x = *reinterpret_cast<const uint4*>(stage + j * 32 + piece * 8);
+            if (m < p.rowsB && n < p.rowsA) {
+              if (p.gate) {
+                const uint4 g = *reinterpret_cast<const uint4*>(p.gate + static_cast<int64_t>(m) * p.ldg + n);
+                x.x &= bf16_pos_mask(g.x);
+                x.y &= bf16_pos_mask(g.y);
+                x.z &= bf16_pos_mask(g.z);
+                x.w &= bf16_pos_mask(g.w);
+              }
+              if (p.a24_vals) {
+                const uint32_t n0 = pick2_nibble(x.x, x.y);
+                const uint32_t n1 = pick2_nibble(x.z, x.w);
+                const uint32_t k0 = kept_pair(x.x, x.y, n0);
+                const uint32_t k1 = kept_pair(x.z, x.w, n1);
+                mask_group(x.x, x.y, n0);
+                mask_group(x.z, x.w, n1);
+                *reinterpret_cast<uint2*>(p.a24_vals + static_cast<int64_t>(m) * p.a24_ldv + n / 2) =
+                    make_uint2(k0, k1);
+                p.a24_meta[static_cast<int64_t>(m) * p.a24_ldm + n / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
+              }
+              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
+            }
+          }
+          __syncwarp();
+        }
+      } else {
+        // out[a_row, j]: A row = token, B row = output feature
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(acc + c * 32, v);
+          tc_wait_ld();
+          const int n0 = tb * BN + c * 32;
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
+            if (p.bias) {
+              f0 += (n0 + 2 * j < p.rowsB) ? p.bias[n0 + 2 * j] : 0.f;
+              f1 += (n0 + 2 * j + 1 < p.rowsB) ? p.bias[n0 + 2 * j + 1] : 0.f;
+            }
+            if (p.relu) {
+              f0 = fmaxf(f0, 0.f);
+              f1 = fmaxf(f1, 0.f);
+            }
+            w[j] = pack_bf16x2(f0, f1);
+          }
+          if (a_row < p.rowsA) {
+            __nv_bfloat16* o = p.out + static_cast<int64_t>(a_row) * p.ldo + n0;
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc)
+              if (n0 + pc * 8 < p.rowsB)
+                *reinterpret_cast<uint4*>(o + pc * 8) =
+                    make_uint4(w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- masked dW GEMM
+// Per stage (64 tokens): A = dY tile [64 tokens x 128 features] as two 64-wide
+// boxes, B = X tile [64 tokens x 256 columns] as four 64-wide boxes; 128B
+// swizzle, MN-major for both operands.
+template <int STAGES>
+struct DwSmem {
+  static constexpr int kA = 64 * 128 * 2;
+  static constexpr int kB = 64 * 256 * 2;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + STAGES * kA;
+  static constexpr int kOffBar = kOffB + STAGES * kB;
+  static constexpr int kBytes = kOffBar + 8 * (2 * STAGES + 5) + 16;
+  static constexpr int kTx = kA + kB;
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    dw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const DwParams p) {
+  using L = DwSmem<STAGES>;
+  constexpr int BN = 256;
+  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false, /*a_mn=*/true, /*b_mn=*/true);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* spare = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(spare, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int ta, tb;
+        tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], L::kTx);
+          uint8_t* a = smem + L::kOffA + s * L::kA;
+          uint8_t* b = smem + L::kOffB + s * L::kB;
+          for (int i = 0; i < 2; ++i) tma_load_2d(a + i * 8192, &tmA, &full[s], ta * kBM + i * 64, kb * 64);
+          for (int i = 0; i < 4; ++i) tma_load_2d(b + i * 8192, &tmB, &full[s], tb * BN + i * 64, kb * 64);
+        }
+      }
+      const uint32_t n_drain = it < STAGES ? it : STAGES;
+      for (uint32_t i = 0; i < n_drain; ++i) {
+        const uint32_t j = it - 1 - i;
+        p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    uint32_t it = 0, tl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1;
+      if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + b * BN;
+      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!p24_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
+          const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = smem_desc(a_base + kk * 2048, 8192, 1024, kSwizzle128B);
+            const uint64_t bdesc = smem_desc(b_base + kk * 2048, 8192, 1024, kSwizzle128B);
+            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&acc_full[b]);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      tc_commit(spare);
+      p24_wait_quiet(spare, 0);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    uint32_t tl = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
+      int ta, tb;
+      tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      const int b = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1;
+      if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + b * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const int n = ta * kBM + q * 32 + lane;  // row of dW
+      const bool row_ok = n < p.N;
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(acc + c * 32, v);
+        tc_wait_ld();
+        const int k0 = tb * BN + c * 32;
+        if (row_ok && k0 < p.K) {
+          const int nbytes = min(4, (p.K - k0) / 8);  // 8 columns per metadata byte
+          uint32_t mw = 0;
+          const uint8_t* mrow = p.meta + static_cast<int64_t>(n) * p.ldm + k0 / 8;
+          if (nbytes == 4) mw = *reinterpret_cast<const uint32_t*>(mrow);
+          else
+            for (int i = 0; i < nbytes; ++i) mw |= static_cast<uint32_t>(mrow[i]) << (8 * i);
+          uint32_t w[16];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t nib = (mw >> (4 * g)) & 0xFu;
+            const uint32_t kbits = (1u << (nib & 3u)) | (1u << (nib >> 2));
+            float f[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[i] = (kbits >> i) & 1u ? __uint_as_float(v[4 * g + i]) : 0.f;
+            w[2 * g] = pack_bf16x2(f[0], f[1]);
+            w[2 * g + 1] = pack_bf16x2(f[2], f[3]);
+          }
+          __nv_bfloat16* o = p.out + static_cast<int64_t>(n) * p.ldo + k0;
+#pragma unroll
+          for (int pc = 0; pc < 4; ++pc)
+            if (k0 + pc * 8 < p.K)
+              *reinterpret_cast<uint4*>(o + pc * 8) =
+                  make_uint4(w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  (void)elem_bytes;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+constexpr int kSpBN = 224;
+constexpr int kSpStages = 5;
+constexpr int kDwStages = 4;
+
+template <bool kTrans>
+cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const SpmmParams& p,
+                     cudaStream_t s) {
+  using L = SpmmSmem<kSpBN, kSpStages>;
+  auto kern = spmm_kernel<kSpBN, kSpStages, kTrans>;
+  const int smem = L::kBytes + 1024;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const int grid = std::min(p.num_tiles, num_sms());
+  kern<<<grid, 320, smem, s>>>(a, b, e, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out, int64_t ldo,
+                        bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s) {
+  if (A.rows == 0 || rowsB == 0) return cudaSuccess;
+  SpmmParams p{};
+  p.rowsA = static_cast<int>(A.rows);
+  p.rowsB = static_cast<int>(rowsB);
+  p.K = static_cast<int>(A.cols);
+  p.tilesA = static_cast<int>((A.rows + kBM - 1) / kBM);
+  p.tilesB = static_cast<int>((rowsB + kSpBN - 1) / kSpBN);
+  p.num_tiles = p.tilesA * p.tilesB;
+  p.group = std::min(p.tilesA, 16);
+  p.nkb = static_cast<int>((A.cols + 63) / 64);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.ldo = ldo;
+  p.bias = epi.bias;
+  p.relu = epi.relu ? 1 : 0;
+  p.gate = static_cast<const uint16_t*>(epi.gate);
+  p.ldg = epi.ldg;
+  p.a24_vals = static_cast<uint16_t*>(epi.act24.vals);
+  p.a24_ldv = epi.act24.ldv;
+  p.a24_meta = epi.act24.meta;
+  p.a24_ldm = epi.act24.ldm;
+  p.status = status;
+  if (A.cols == 0) return cudaErrorInvalidValue;
+
+  CUtensorMap ta, tb, te;
+  if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 32, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64, kSpBN,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  return transposed_out ? run_spmm<true>(ta, tb, te, p, s) : run_spmm<false>(ta, tb, te, p, s);
+}
+
+cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
+                             int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
+                             cudaStream_t s) {
+  if (N == 0 || K == 0) return cudaSuccess;
+  if (M == 0) {
+    // empty reduction: dW = 0 everywhere
+    return cudaMemset2DAsync(dW, lddw * 2, 0, K * 2, N, s);
+  }
+  DwParams p{};
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.M = static_cast<int>(M);
+  p.tilesA = static_cast<int>((N + kBM - 1) / kBM);
+  p.tilesB = static_cast<int>((K + 255) / 256);
+  p.num_tiles = p.tilesA * p.tilesB;
+  p.group = std::min(p.tilesA, 16);
+  p.nkb = static_cast<int>((M + 63) / 64);
+  p.out = static_cast<__nv_bfloat16*>(dW);
+  p.ldo = lddw;
+  p.meta = meta;
+  p.ldm = ldm;
+  p.status = status;
+  CUtensorMap ta, tb;
+  if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dY, N, M, lddy * 2, 64, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  using L = DwSmem<kDwStages>;
+  auto kern = dw_kernel<kDwStages>;
+  const int smem = L::kBytes + 1024;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const int grid = std::min(p.num_tiles, num_sms());
+  kern<<<grid, 192, smem, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace p24

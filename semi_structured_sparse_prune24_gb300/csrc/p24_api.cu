@@ -1,0 +1,338 @@
+// p24_api.cu -- the extern "C" entry points of libprune24 declared in
+// include/prune24.h: host-side validation (nothing is launched on an error),
+// workspace carving for the FFN step, and the device status word.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "p24_internal.h"
+
+namespace p24 {
+namespace {
+
+__device__ int g_status;  // P24_OK, or P24_ETIMEOUT after a bounded wait expired
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dense(const void* p, int64_t rows, int64_t cols, int64_t ld) {
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return P24_EINVAL;
+  if (rows == 0 || cols == 0) return P24_OK;
+  if (!p) return P24_EINVAL;
+  if (ld < cols) return P24_EINVAL;
+  if (!aligned16(p) || (ld % 8) != 0) return P24_EALIGN;
+  return P24_OK;
+}
+
+int check_sparse(const p24_sparse* d) {
+  if (!d) return P24_EINVAL;
+  if (d->rows < 0 || d->cols < 0 || d->rows > kMaxDim || d->cols > kMaxDim) return P24_EINVAL;
+  if (d->cols % 4 != 0) return P24_EINVAL;
+  if (d->rows == 0 || d->cols == 0) return P24_OK;
+  if (!d->vals || !d->meta) return P24_EINVAL;
+  if (d->ldv < p24_ld_vals(d->cols) || d->ldm < p24_ld_meta(d->cols)) return P24_EINVAL;
+  if (!aligned16(d->vals) || !aligned16(d->meta) || d->ldv % 8 != 0 || d->ldm % 16 != 0) return P24_EALIGN;
+  return P24_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? P24_OK : P24_ECUDA; }
+
+#define P24_TRY(expr)              \
+  do {                             \
+    const int _rc = (expr);        \
+    if (_rc != P24_OK) return _rc; \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace of ffn24_step, carved in this order (each region 256-byte aligned).
+struct StepLayout {
+  p24_sparse up_fwd, up_bwdT, dn_fwd, dn_bwdT, hs;
+  size_t off[16];
+  size_t total;
+};
+
+void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, char* base, StepLayout& L,
+                 void** wdm, void** dH, float** cs) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + off : nullptr;
+    off = round_up(off + bytes, 256);
+    return static_cast<void*>(p);
+  };
+  auto sparse = [&](p24_sparse& s, int64_t rows, int64_t cols) {
+    s.rows = rows;
+    s.cols = cols;
+    s.ldv = p24_ld_vals(cols);
+    s.ldm = p24_ld_meta(cols);
+    s.vals = take(static_cast<size_t>(rows * s.ldv * 2));
+    s.meta = static_cast<uint8_t*>(take(static_cast<size_t>(rows * s.ldm)));
+  };
+  sparse(L.up_fwd, ffn, d);
+  sparse(L.up_bwdT, d, ffn);
+  sparse(L.dn_fwd, d, ffn);
+  sparse(L.dn_bwdT, ffn, d);
+  if (flags & P24_STEP_ACT24) {
+    sparse(L.hs, M, ffn);
+    *wdm = take(static_cast<size_t>(d * ffn * 2));
+  } else {
+    std::memset(&L.hs, 0, sizeof(L.hs));
+    *wdm = nullptr;
+  }
+  *dH = take(static_cast<size_t>(M * ffn * 2));
+  const int64_t S = colsum_slabs(M);
+  *cs = static_cast<float*>(take(static_cast<size_t>(S * (ffn > d ? ffn : d) * 4)));
+  L.total = off;
+}
+
+}  // namespace
+
+int* device_status_ptr() {
+  int* p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status) != cudaSuccess) return nullptr;
+  return p;
+}
+
+}  // namespace p24
+
+using namespace p24;
+
+extern "C" {
+
+int64_t p24_ld_vals(int64_t cols) { return ((cols / 2) + 7) / 8 * 8; }
+int64_t p24_ld_meta(int64_t cols) { return 16 * ((cols + 127) / 128); }
+
+int prune24_compress(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse* out, void* W_masked,
+                     int64_t ldwm, void* stream) {
+  if (cols % 4 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(W, rows, cols, ldw));
+  P24_TRY(check_sparse(out));
+  if (out->rows != rows || out->cols != cols) return P24_EINVAL;
+  if (W_masked) P24_TRY(check_dense(W_masked, rows, cols, ldwm));
+  return cuda_status(launch_compress(W, rows, cols, ldw, *out, W_masked, ldwm, as_stream(stream)));
+}
+
+int prune24_transpose_repack(const p24_sparse* fwd, const p24_sparse* bwdT, void* stream) {
+  P24_TRY(check_sparse(fwd));
+  P24_TRY(check_sparse(bwdT));
+  if (fwd->rows % 4 != 0) return P24_EINVAL;
+  if (bwdT->rows != fwd->cols || bwdT->cols != fwd->rows) return P24_EINVAL;
+  return cuda_status(launch_transpose_repack(*fwd, *bwdT, as_stream(stream)));
+}
+
+int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse* fwd,
+                          const p24_sparse* bwdT, void* W_masked, int64_t ldwm, void* stream) {
+  if (cols % 4 != 0 || rows % 4 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(W, rows, cols, ldw));
+  P24_TRY(check_sparse(fwd));
+  P24_TRY(check_sparse(bwdT));
+  if (fwd->rows != rows || fwd->cols != cols || bwdT->rows != cols || bwdT->cols != rows) return P24_EINVAL;
+  if (W_masked) P24_TRY(check_dense(W_masked, rows, cols, ldwm));
+  return cuda_status(launch_compress_both(W, rows, cols, ldw, *fwd, *bwdT, W_masked, ldwm, as_stream(stream)));
+}
+
+int spmm24_fwd(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const float* bias, uint32_t flags,
+               void* Y, int64_t ldy, const p24_sparse* Y24, void* stream) {
+  if (flags & ~(P24_EPI_BIAS | P24_EPI_RELU | P24_EPI_ACT24)) return P24_EINVAL;
+  P24_TRY(check_sparse(W));
+  const int64_t N = W->rows, K = W->cols;
+  if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(X, M, K, ldx));
+  P24_TRY(check_dense(Y, M, N, ldy));
+  if ((flags & P24_EPI_BIAS) && !bias) return P24_EINVAL;
+  EpiArgs epi;
+  epi.bias = (flags & P24_EPI_BIAS) ? bias : nullptr;
+  epi.relu = (flags & P24_EPI_RELU) != 0;
+  if (flags & P24_EPI_ACT24) {
+    P24_TRY(check_sparse(Y24));
+    if (Y24->rows != M || Y24->cols != N) return P24_EINVAL;
+    epi.act24 = *Y24;
+  }
+  if (M == 0 || N == 0) return P24_OK;
+  if (K == 0) return P24_EUNSUPPORTED;
+  const cudaStream_t s = as_stream(stream);
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  P24_TRY(cuda_status(launch_spmm(*W, X, M, ldx, Y, ldy, /*transposed_out=*/true, epi, st, s)));
+  if (flags & P24_EPI_ACT24) return cuda_status(launch_pad(*Y24, s));
+  return P24_OK;
+}
+
+int spmm24_fwd_sparse_act(const p24_sparse* Xs, const void* Wm, int64_t N, int64_t ldw, const float* bias,
+                          uint32_t flags, void* Y, int64_t ldy, void* stream) {
+  if (flags & ~(P24_EPI_BIAS | P24_EPI_RELU)) return P24_EINVAL;
+  P24_TRY(check_sparse(Xs));
+  const int64_t M = Xs->rows, K = Xs->cols;
+  if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(Wm, N, K, ldw));
+  P24_TRY(check_dense(Y, M, N, ldy));
+  if ((flags & P24_EPI_BIAS) && !bias) return P24_EINVAL;
+  if (M == 0 || N == 0) return P24_OK;
+  if (K == 0) return P24_EUNSUPPORTED;
+  EpiArgs epi;
+  epi.bias = (flags & P24_EPI_BIAS) ? bias : nullptr;
+  epi.relu = (flags & P24_EPI_RELU) != 0;
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_spmm(*Xs, Wm, N, ldw, Y, ldy, /*transposed_out=*/false, epi, st, as_stream(stream)));
+}
+
+int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT, const void* gate, int64_t ldg,
+                  void* dX, int64_t lddx, void* stream) {
+  P24_TRY(check_sparse(WbwdT));
+  const int64_t K = WbwdT->rows, N = WbwdT->cols;
+  if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(dY, M, N, lddy));
+  P24_TRY(check_dense(dX, M, K, lddx));
+  if (gate) P24_TRY(check_dense(gate, M, K, ldg));
+  if (M == 0 || K == 0) return P24_OK;
+  if (N == 0) return P24_EUNSUPPORTED;
+  EpiArgs epi;
+  epi.gate = gate;
+  epi.ldg = ldg;
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_spmm(*WbwdT, dY, M, lddy, dX, lddx, /*transposed_out=*/true, epi, st, as_stream(stream)));
+}
+
+int masked_dw_gemm(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, const p24_sparse* Wfwd,
+                   void* dW, int64_t lddw, void* stream) {
+  P24_TRY(check_sparse(Wfwd));
+  const int64_t N = Wfwd->rows, K = Wfwd->cols;
+  if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(dY, M, N, lddy));
+  P24_TRY(check_dense(X, M, K, ldx));
+  P24_TRY(check_dense(dW, N, K, lddw));
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(
+      launch_masked_dw(dY, lddy, X, ldx, M, N, K, Wfwd->meta, Wfwd->ldm, dW, lddw, st, as_stream(stream)));
+}
+
+size_t p24_colsum_workspace_size(int64_t M, int64_t N) {
+  if (M < 0 || N < 0) return 0;
+  return static_cast<size_t>(colsum_slabs(M) * N * 4);
+}
+
+int p24_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, void* ws, size_t ws_bytes,
+               void* stream) {
+  P24_TRY(check_dense(G, M, N, ldg));
+  if (N > 0 && !out) return P24_EINVAL;
+  if (N > 0 && !aligned16(out)) return P24_EALIGN;
+  if (N > 0 && M > 0) {
+    if (!ws) return P24_EINVAL;
+    if (!aligned16(ws)) return P24_EALIGN;
+    if (ws_bytes < p24_colsum_workspace_size(M, N)) return P24_ENOSPACE;
+  }
+  return cuda_status(launch_colsum(G, M, N, ldg, out, static_cast<float*>(ws), as_stream(stream)));
+}
+
+size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags) {
+  if (M < 0 || d < 0 || ffn < 0) return 0;
+  StepLayout L;
+  void *wdm, *dH;
+  float* cs;
+  step_layout(M, d, ffn, flags, nullptr, L, &wdm, &dH, &cs);
+  return L.total;
+}
+
+int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream) {
+  if (!a) return P24_EINVAL;
+  if (a->flags & ~P24_STEP_ACT24) return P24_EINVAL;
+  const int64_t M = a->M, d = a->d, ffn = a->ffn;
+  if (M < 0 || d <= 0 || ffn <= 0 || d % 8 != 0 || ffn % 8 != 0) return P24_EINVAL;
+  const bool act24 = (a->flags & P24_STEP_ACT24) != 0;
+  P24_TRY(check_dense(a->W_up, ffn, d, d));
+  P24_TRY(check_dense(a->W_down, d, ffn, ffn));
+  P24_TRY(check_dense(a->dW_up, ffn, d, d));
+  P24_TRY(check_dense(a->dW_down, d, ffn, ffn));
+  if (M > 0) {
+    P24_TRY(check_dense(a->X, M, d, d));
+    P24_TRY(check_dense(a->dY, M, d, d));
+    P24_TRY(check_dense(a->Y, M, d, d));
+    P24_TRY(check_dense(a->dX, M, d, d));
+    P24_TRY(check_dense(a->H, M, ffn, ffn));
+  }
+  for (const void* p : {static_cast<const void*>(a->b_up), static_cast<const void*>(a->b_down),
+                        static_cast<const void*>(a->db_up), static_cast<const void*>(a->db_down)})
+    if (p && !aligned16(p)) return P24_EALIGN;
+  if (!workspace) return P24_EINVAL;
+  if (!aligned16(workspace)) return P24_EALIGN;
+  StepLayout L;
+  void *wdm, *dHv;
+  float* cs;
+  step_layout(M, d, ffn, a->flags, static_cast<char*>(workspace), L, &wdm, &dHv, &cs);
+  if (ws_bytes < L.total) return P24_ENOSPACE;
+  const cudaStream_t s = as_stream(stream);
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+
+  // 1. fresh 2:4 masks of both weights, and their double-pruned transposes
+  P24_TRY(cuda_status(launch_compress_both(a->W_up, ffn, d, d, L.up_fwd, L.up_bwdT, nullptr, 0, s)));
+  P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT, wdm, ffn, s)));
+  if (M == 0) {
+    if (a->db_up) P24_TRY(cuda_status(cudaMemsetAsync(a->db_up, 0, ffn * 4, s)));
+    if (a->db_down) P24_TRY(cuda_status(cudaMemsetAsync(a->db_down, 0, d * 4, s)));
+    P24_TRY(cuda_status(cudaMemsetAsync(a->dW_up, 0, ffn * d * 2, s)));
+    return cuda_status(cudaMemsetAsync(a->dW_down, 0, ffn * d * 2, s));
+  }
+  // 2. H = ReLU(X W_up^T + b_up)  [ACT24: pruned 2:4 along ffn, compressed copy in hs]
+  EpiArgs up;
+  up.bias = a->b_up;
+  up.relu = true;
+  if (act24) up.act24 = L.hs;
+  P24_TRY(cuda_status(launch_spmm(L.up_fwd, a->X, M, d, a->H, ffn, true, up, st, s)));
+  if (act24) P24_TRY(cuda_status(launch_pad(L.hs, s)));
+  // 3. Y = H W_down^T + b_down
+  EpiArgs dn;
+  dn.bias = a->b_down;
+  if (act24)
+    P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s)));
+  else
+    P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s)));
+  // 4. dH = (dY W_down_bwd) * [H > 0]
+  EpiArgs g;
+  g.gate = a->H;
+  g.ldg = ffn;
+  P24_TRY(cuda_status(launch_spmm(L.dn_bwdT, a->dY, M, d, dHv, ffn, true, g, st, s)));
+  // 5. bias gradients
+  if (a->db_up) P24_TRY(cuda_status(launch_colsum(dHv, M, ffn, ffn, a->db_up, cs, s)));
+  if (a->db_down) P24_TRY(cuda_status(launch_colsum(a->dY, M, d, d, a->db_down, cs, s)));
+  // 6. dW_down = (dY^T H) on mask(W_down)
+  P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm, a->dW_down,
+                                       ffn, st, s)));
+  // 7. dX = dH W_up_bwd
+  EpiArgs none;
+  P24_TRY(cuda_status(launch_spmm(L.up_bwdT, dHv, M, ffn, a->dX, d, true, none, st, s)));
+  // 8. dW_up = (dH^T X) on mask(W_up)
+  return cuda_status(
+      launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s));
+}
+
+int p24_query_status(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return P24_ECUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return P24_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return P24_ECUDA;
+  return v;
+}
+
+const char* p24_strerror(int code) {
+  switch (code) {
+    case P24_OK: return "ok";
+    case P24_EINVAL: return "invalid argument (null pointer, shape or flag)";
+    case P24_EALIGN: return "pointer or row stride not 16-byte aligned";
+    case P24_ECUDA: return "CUDA call or kernel launch failed";
+    case P24_ETIMEOUT: return "a kernel's bounded wait expired";
+    case P24_EUNSUPPORTED: return "unsupported device or shape";
+    case P24_ENOSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// p24_internal.h -- host-side launchers shared between the translation units
+// of libprune24 (not part of the public ABI; see include/prune24.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "prune24.h"
+
+namespace p24 {
+
+// ---- pruning / packing (prune24_kernels.cu) ----
+cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& out,
+                            void* W_masked, int64_t ldwm, cudaStream_t s);
+cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& fwd,
+                                 const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s);
+cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s);
+cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s);
+int64_t colsum_slabs(int64_t M);
+cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s);
+
+// ---- tensor-core GEMMs (gemm24_kernels.cu) ----
+struct EpiArgs {
+  const float* bias = nullptr;  // fp32 per output column (of Y), or null
+  bool relu = false;
+  const void* gate = nullptr;   // bf16 [M, ldg] ReLU output for the backward gate, or null
+  int64_t ldg = 0;
+  p24_sparse act24{};           // compressed activation output (vals != null => enabled)
+};
+
+// C[i, j] = sum_r A[i, r] * B[j, r] with A 2:4-sparse (compressed, K-major) and
+// B dense K-major; written transposed (out[j, i]) when `transposed_out`.
+cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out,
+                        int64_t ldo, bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s);
+
+// dW[n, k] = sum_m dY[m, n] * X[m, k] on mask(meta) (both operands MN-major).
+cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
+                             int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
+                             cudaStream_t s);
+
+int* device_status_ptr();  // the status word of the current device
+
+}  // namespace p24

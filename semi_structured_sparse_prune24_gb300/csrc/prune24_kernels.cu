@@ -1,0 +1,364 @@
+// prune24_kernels.cu -- HBM-bound kernels of the 2:4 path: magnitude pruning
+// + compression, the double prune of the transposed weight, padding of
+// compressed rows, and deterministic column sums (bias gradients).
+//
+// Method (inno4scale "Success story ESPLAG", "Solution": N:M pruning with a
+// compressed storage format; SLOPE abstract, NSF PAR award 2340011: the
+// transposed weight is pruned again with N:M for the backward pass):
+// in each group of 4 consecutive values the two of largest magnitude are kept;
+// magnitude = bf16 bits with the sign cleared; ties go to the lower index.
+// Every decision is integer, so the outputs are a pure function of the input bits.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "p24_internal.h"
+
+namespace p24 {
+namespace {
+
+// ---------------------------------------------------------------- the 2:4 pick
+// A group of four bf16 values is held as two 32-bit words: lo = e0 | e1 << 16,
+// hi = e2 | e3 << 16. Each value gets a composite key (magnitude << 2) | (3 - i):
+// distinct for the four positions, larger = kept first, and among equal
+// magnitudes the lower index has the larger key. The two largest composites
+// come out of a 4-input max/min network.
+__device__ __forceinline__ uint32_t pick2_nibble(uint32_t lo, uint32_t hi) {
+  const uint32_t c0 = ((lo & 0x7FFFu) << 2) | 3u;
+  const uint32_t c1 = ((lo >> 14) & 0x1FFFCu) | 2u;
+  const uint32_t c2 = ((hi & 0x7FFFu) << 2) | 1u;
+  const uint32_t c3 = (hi >> 14) & 0x1FFFCu;
+  const uint32_t a = max(c0, c1), b = min(c0, c1);
+  const uint32_t c = max(c2, c3), d = min(c2, c3);
+  const uint32_t top = max(a, c);
+  const uint32_t second = max(min(a, c), max(b, d));
+  const uint32_t i_top = 3u - (top & 3u), i_sec = 3u - (second & 3u);
+  return min(i_top, i_sec) | (max(i_top, i_sec) << 2);
+}
+
+// The two kept values (ascending index) packed as v0 | v1 << 16.
+__device__ __forceinline__ uint32_t kept_pair(uint32_t lo, uint32_t hi, uint32_t nib) {
+  const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+  const uint32_t sel = 0x1010u + i0 * 0x22u + i1 * 0x2200u;  // bytes 2i0,2i0+1,2i1,2i1+1
+  return __byte_perm(lo, hi, sel);
+}
+
+// The group with its dropped values set to +0.
+__device__ __forceinline__ void masked_group(uint32_t lo, uint32_t hi, uint32_t nib, uint32_t& mlo,
+                                             uint32_t& mhi) {
+  const uint32_t kb = (1u << (nib & 3u)) | (1u << (nib >> 2));
+  mlo = lo & (((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u));
+  mhi = hi & (((kb & 4u) ? 0x0000FFFFu : 0u) | ((kb & 8u) ? 0xFFFF0000u : 0u));
+}
+
+// Scatter two kept values back into a dense group.
+__device__ __forceinline__ void expand_group(uint32_t pair, uint32_t nib, uint32_t& lo, uint32_t& hi) {
+  const uint32_t i0 = nib & 3u, i1 = (nib >> 2) & 3u;
+  const uint64_t v = (static_cast<uint64_t>(pair & 0xFFFFu) << (16u * i0)) |
+                     (static_cast<uint64_t>(pair >> 16) << (16u * i1));
+  lo = static_cast<uint32_t>(v);
+  hi = static_cast<uint32_t>(v >> 32);
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+// ---------------------------------------------------------------- compress
+// One thread = one 16-byte piece (8 values, 2 groups) per step; a CTA of 256
+// threads covers 1024 consecutive pieces of a row, 4 per thread, loads first.
+template <bool kMasked>
+__global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restrict__ W, int64_t rows, int64_t cols,
+                                                       int64_t ldw, uint16_t* __restrict__ vals, int64_t ldv,
+                                                       uint8_t* __restrict__ meta, int64_t ldm,
+                                                       uint16_t* __restrict__ Wm, int64_t ldwm) {
+  for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const uint16_t* w = W + row * ldw;
+    const int64_t p0 = static_cast<int64_t>(blockIdx.x) * 1024 + threadIdx.x;
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t e = (p0 + j * 256) * 8;
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (e + 8 <= cols) {
+        v[j] = ld_stream_v4(w + e);
+      } else if (e + 4 <= cols) {
+        const uint2 h = __ldcs(reinterpret_cast<const uint2*>(w + e));
+        v[j].x = h.x;
+        v[j].y = h.y;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t p = p0 + j * 256;
+      const int64_t e = p * 8;
+      if (e + 4 > cols) continue;
+      const uint32_t n0 = pick2_nibble(v[j].x, v[j].y);
+      const uint32_t k0 = kept_pair(v[j].x, v[j].y, n0);
+      if (e + 8 <= cols) {
+        const uint32_t n1 = pick2_nibble(v[j].z, v[j].w);
+        const uint32_t k1 = kept_pair(v[j].z, v[j].w, n1);
+        *reinterpret_cast<uint2*>(vals + row * ldv + p * 4) = make_uint2(k0, k1);
+        meta[row * ldm + p] = static_cast<uint8_t>(n0 | (n1 << 4));
+        if (kMasked) {
+          uint4 m;
+          masked_group(v[j].x, v[j].y, n0, m.x, m.y);
+          masked_group(v[j].z, v[j].w, n1, m.z, m.w);
+          *reinterpret_cast<uint4*>(Wm + row * ldwm + e) = m;
+        }
+      } else {
+        *reinterpret_cast<uint32_t*>(vals + row * ldv + p * 4) = k0;
+        meta[row * ldm + p] = static_cast<uint8_t>(n0 | 0x40u);  // odd group count: pad high nibble
+        if (kMasked) {
+          uint2 m;
+          masked_group(v[j].x, v[j].y, n0, m.x, m.y);
+          *reinterpret_cast<uint2*>(Wm + row * ldwm + e) = m;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- double prune
+// One warp = one 32-column chunk of a 128-row block; lane l owns the row quad
+// 4h..4h+3 (h = block*32 + l). It holds the quad's 4 x 32 forward-masked values
+// in registers, so each of the 32 column groups (4 rows, one column) is pruned
+// without shared memory, and lanes write consecutive groups of a W_bwd^T row.
+// kFromDense: the input is the dense W (the forward prune happens here too);
+// otherwise the input is the compressed forward matrix.
+template <bool kFromDense, bool kMasked>
+__global__ void __launch_bounds__(256) double_prune_kernel(
+    const uint16_t* __restrict__ W, int64_t ldw,                       // dense input (kFromDense)
+    const uint16_t* __restrict__ fv_in, uint16_t* __restrict__ fv_out,  // forward vals (in / out)
+    int64_t ldfv,
+    const uint8_t* __restrict__ fm_in, uint8_t* __restrict__ fm_out,   // forward meta (in / out)
+    int64_t ldfm, int64_t rows, int64_t cols,
+    uint16_t* __restrict__ tv, int64_t ldtv, uint8_t* __restrict__ tm, int64_t ldtm,
+    uint16_t* __restrict__ Wm, int64_t ldwm) {
+  const int lane = threadIdx.x & 31;
+  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int64_t c0 = chunk * 32;
+  if (c0 >= cols) return;  // uniform per warp
+  const int64_t nquads = rows / 4;
+  const int64_t ngroups_t = nquads;  // groups per W_bwd^T row
+
+  for (int64_t qb = blockIdx.y; qb * 32 < nquads; qb += gridDim.y) {
+    const int64_t h = qb * 32 + lane;
+    const bool active = h < nquads;
+    uint32_t d[4][16];  // [row of quad][word]: word w holds columns c0+2w, c0+2w+1
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t row = 4 * h + r;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {  // 8-column pieces
+        const int64_t e = c0 + 8 * p;
+        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+        const bool full = active && e + 8 <= cols;
+        const bool half = active && !full && e + 4 <= cols;
+        if (kFromDense) {
+          if (full) {
+            const uint4 x = ld_stream_v4(W + row * ldw + e);
+            w0 = x.x; w1 = x.y; w2 = x.z; w3 = x.w;
+          } else if (half) {
+            const uint2 x = __ldcs(reinterpret_cast<const uint2*>(W + row * ldw + e));
+            w0 = x.x; w1 = x.y;
+          }
+          if (full || half) {
+            const uint32_t n0 = pick2_nibble(w0, w1);
+            const uint32_t k0 = kept_pair(w0, w1, n0);
+            uint32_t n1 = 0x4u, k1 = 0;
+            if (full) {
+              n1 = pick2_nibble(w2, w3);
+              k1 = kept_pair(w2, w3, n1);
+            }
+            masked_group(w0, w1, n0, w0, w1);
+            if (full) masked_group(w2, w3, n1, w2, w3);
+            uint16_t* vout = fv_out + row * ldfv + e / 2;
+            if (full) *reinterpret_cast<uint2*>(vout) = make_uint2(k0, k1);
+            else *reinterpret_cast<uint32_t*>(vout) = k0;
+            fm_out[row * ldfm + e / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
+            if (kMasked) {
+              if (full) *reinterpret_cast<uint4*>(Wm + row * ldwm + e) = make_uint4(w0, w1, w2, w3);
+              else *reinterpret_cast<uint2*>(Wm + row * ldwm + e) = make_uint2(w0, w1);
+            }
+          }
+        } else {
+          if (full || half) {
+            const uint32_t mb = fm_in[row * ldfm + e / 8];
+            if (full) {
+              const uint2 pr = *reinterpret_cast<const uint2*>(fv_in + row * ldfv + e / 2);
+              expand_group(pr.x, mb & 0xFu, w0, w1);
+              expand_group(pr.y, mb >> 4, w2, w3);
+            } else {
+              const uint32_t pr = *reinterpret_cast<const uint32_t*>(fv_in + row * ldfv + e / 2);
+              expand_group(pr, mb & 0xFu, w0, w1);
+            }
+          }
+        }
+        d[r][4 * p + 0] = w0;
+        d[r][4 * p + 1] = w1;
+        d[r][4 * p + 2] = w2;
+        d[r][4 * p + 3] = w3;
+      }
+    }
+    // Column groups: column c0+k, rows 4h..4h+3.
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int64_t col = c0 + k;
+      if (col >= cols) break;  // uniform per warp
+      const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
+      const uint32_t lo = __byte_perm(d[0][k >> 1], d[1][k >> 1], sel);
+      const uint32_t hi = __byte_perm(d[2][k >> 1], d[3][k >> 1], sel);
+      const uint32_t nib = pick2_nibble(lo, hi);
+      const uint32_t pair = kept_pair(lo, hi, nib);
+      const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
+      if (active) {
+        *reinterpret_cast<uint32_t*>(tv + col * ldtv + 2 * h) = pair;
+        if ((lane & 1) == 0) {
+          const uint32_t hiNib = (h + 1 < ngroups_t) ? nib_next : 0x4u;
+          tm[col * ldtm + h / 2] = static_cast<uint8_t>(nib | (hiNib << 4));
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- padding
+// Zero values past cols/2 and 0x4 nibbles past the last group, up to the strides.
+__global__ void pad_kernel(uint16_t* __restrict__ vals, int64_t ldv, uint8_t* __restrict__ meta, int64_t ldm,
+                           int64_t rows, int64_t cols) {
+  const int64_t nv = ldv - cols / 2;
+  const int64_t groups = cols / 4;
+  const int64_t mb0 = (groups + 1) / 2;  // first byte with no data nibble
+  const int64_t nm = ldm - mb0;
+  const int64_t per_row = nv + nm;
+  const int64_t total = rows * per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row, j = i % per_row;
+    if (j < nv) vals[r * ldv + cols / 2 + j] = 0;
+    else meta[r * ldm + mb0 + (j - nv)] = 0x44;
+  }
+}
+
+// ---------------------------------------------------------------- column sums
+// Pass 1: slab s of rows, 2 columns per thread, fp32 sums in row order.
+__global__ void __launch_bounds__(256) colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int64_t M,
+                                                             int64_t N, int64_t ldg, int64_t rows_per_slab,
+                                                             float* __restrict__ part) {
+  const int64_t col = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 2;
+  const int64_t s = blockIdx.y;
+  if (col >= N) return;
+  const int64_t r0 = s * rows_per_slab;
+  const int64_t r1 = min(M, r0 + rows_per_slab);
+  float a0 = 0.f, a1 = 0.f;
+  if (col + 1 < N) {
+    for (int64_t r = r0; r < r1; ++r) {
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(G + r * ldg + col);
+      a0 += __bfloat162float(v.x);
+      a1 += __bfloat162float(v.y);
+    }
+    part[s * N + col] = a0;
+    part[s * N + col + 1] = a1;
+  } else {
+    for (int64_t r = r0; r < r1; ++r) a0 += __bfloat162float(G[r * ldg + col]);
+    part[s * N + col] = a0;
+  }
+}
+
+// Pass 2: fixed-order sum over slabs.
+__global__ void colsum_final_kernel(const float* __restrict__ part, int64_t S, int64_t N, float* __restrict__ out) {
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (col >= N) return;
+  float a = 0.f;
+  for (int64_t s = 0; s < S; ++s) a += part[s * N + col];
+  out[col] = a;
+}
+
+inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n < 1 ? 1 : n) : 65535); }
+
+}  // namespace
+
+cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s) {
+  const int64_t per_row = (d.ldv - d.cols / 2) + (d.ldm - (d.cols / 4 + 1) / 2);
+  if (per_row <= 0 || d.rows == 0) return cudaSuccess;
+  const int64_t total = d.rows * per_row;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 16);
+  pad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<uint16_t*>(d.vals), d.ldv, d.meta, d.ldm,
+                                                           d.rows, d.cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& out,
+                            void* W_masked, int64_t ldwm, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t pieces = (cols + 7) / 8;
+  dim3 grid(static_cast<unsigned>((pieces + 1023) / 1024), grid_y(rows));
+  const auto* w = static_cast<const uint16_t*>(W);
+  auto* v = static_cast<uint16_t*>(out.vals);
+  if (W_masked)
+    compress_kernel<true><<<grid, 256, 0, s>>>(w, rows, cols, ldw, v, out.ldv, out.meta, out.ldm,
+                                               static_cast<uint16_t*>(W_masked), ldwm);
+  else
+    compress_kernel<false><<<grid, 256, 0, s>>>(w, rows, cols, ldw, v, out.ldv, out.meta, out.ldm, nullptr, 0);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_pad(out, s);
+}
+
+cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& fwd,
+                                 const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t chunks = (cols + 31) / 32;
+  const int64_t qblocks = (rows / 4 + 31) / 32;
+  dim3 grid(static_cast<unsigned>((chunks + 7) / 8), grid_y(qblocks));
+  const auto* w = static_cast<const uint16_t*>(W);
+  if (W_masked)
+    double_prune_kernel<true, true><<<grid, 256, 0, s>>>(
+        w, ldw, nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm, rows, cols,
+        static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, static_cast<uint16_t*>(W_masked), ldwm);
+  else
+    double_prune_kernel<true, false><<<grid, 256, 0, s>>>(
+        w, ldw, nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm, rows, cols,
+        static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = launch_pad(fwd, s)) != cudaSuccess) return e;
+  return launch_pad(bwdT, s);
+}
+
+cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s) {
+  const int64_t rows = fwd.rows, cols = fwd.cols;
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t chunks = (cols + 31) / 32;
+  const int64_t qblocks = (rows / 4 + 31) / 32;
+  dim3 grid(static_cast<unsigned>((chunks + 7) / 8), grid_y(qblocks));
+  double_prune_kernel<false, false><<<grid, 256, 0, s>>>(
+      nullptr, 0, static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm, rows, cols,
+      static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_pad(bwdT, s);
+}
+
+int64_t colsum_slabs(int64_t M) {
+  int64_t S = (M + 63) / 64;
+  if (S > 1024) S = 1024;
+  if (S < 1) S = 1;
+  return S;
+}
+
+cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  if (M == 0) return cudaMemsetAsync(out, 0, N * sizeof(float), s);
+  const int64_t S = colsum_slabs(M);
+  const int64_t rps = (M + S - 1) / S;
+  dim3 grid(static_cast<unsigned>((N + 511) / 512), static_cast<unsigned>(S));
+  colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), M, N, ldg, rps, ws);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colsum_final_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(ws, S, N, out);
+  return cudaGetLastError();
+}
+
+}  // namespace p24

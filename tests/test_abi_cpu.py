@@ -1,0 +1,102 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/prune24.h declares, computes its stride helpers, and rejects bad
+arguments on the host before touching CUDA."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def native():
+    from semi_structured_sparse_prune24_gb300 import _native
+    return _native
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "prune24.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\*?\s*([A-Za-z_]\w*)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("prune24_compress", "prune24_transpose_repack", "spmm24_fwd", "spmm24_bwd_dx",
+                     "masked_dw_gemm", "ffn24_step"):
+        assert required in names
+
+
+def test_every_declared_function_is_exported(native):
+    lib = C.CDLL(native._LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_stride_helpers(native):
+    L = native.lib
+    assert L.p24_ld_vals(8200) == 4104 and L.p24_ld_meta(8200) == 1040
+    assert L.p24_ld_vals(512) == 256 and L.p24_ld_meta(512) == 64
+    assert L.p24_ld_vals(4) == 8 and L.p24_ld_meta(4) == 16
+    for cols in range(4, 2000, 4):
+        assert L.p24_ld_vals(cols) >= cols // 2 and L.p24_ld_vals(cols) % 8 == 0
+        assert L.p24_ld_meta(cols) * 2 >= cols // 4 and L.p24_ld_meta(cols) % 16 == 0
+
+
+def test_strerror(native):
+    for code in range(-6, 1):
+        assert native.lib.p24_strerror(code)
+    assert b"unknown" in native.lib.p24_strerror(-99)
+
+
+def _sp(vals, meta, rows, cols, ldv, ldm, native):
+    return native.p24_sparse(vals, meta, rows, cols, ldv, ldm)
+
+
+def test_host_validation_rejects_before_launch(native):
+    L = native.lib
+    EINVAL, EALIGN = native.P24_EINVAL, native.P24_EALIGN
+    fake = 0x10000  # never dereferenced: every call below fails validation first
+    good = _sp(fake, fake, 8, 16, 8, 16, native)
+    # null input
+    assert L.prune24_compress(None, 8, 16, 16, C.byref(good), None, 0, None) == EINVAL
+    # cols not a multiple of 4
+    assert L.prune24_compress(fake, 8, 18, 24, C.byref(good), None, 0, None) == EINVAL
+    # misaligned input pointer / stride
+    assert L.prune24_compress(fake + 2, 8, 16, 16, C.byref(good), None, 0, None) == EALIGN
+    assert L.prune24_compress(fake, 8, 16, 20, C.byref(good), None, 0, None) == EALIGN
+    # output descriptor with a too-small metadata stride
+    bad = _sp(fake, fake, 8, 16, 8, 8, native)
+    assert L.prune24_compress(fake, 8, 16, 16, C.byref(bad), None, 0, None) == EINVAL
+    # shape mismatch between input and descriptor
+    assert L.prune24_compress(fake, 4, 16, 16, C.byref(good), None, 0, None) == EINVAL
+    # repack needs rows % 4 == 0 and transposed shapes
+    odd = _sp(fake, fake, 6, 16, 8, 16, native)
+    t = _sp(fake, fake, 16, 6, 8, 16, native)
+    assert L.prune24_transpose_repack(C.byref(odd), C.byref(t), None) == EINVAL
+    # GEMMs: bad flags, missing bias, K % 8
+    w = _sp(fake, fake, 16, 16, 8, 16, native)
+    assert L.spmm24_fwd(fake, 8, 16, C.byref(w), None, 0x80, fake, 16, None, None) == EINVAL
+    assert L.spmm24_fwd(fake, 8, 16, C.byref(w), None, native.P24_EPI_BIAS, fake, 16, None, None) == EINVAL
+    w12 = _sp(fake, fake, 16, 12, 8, 16, native)
+    assert L.spmm24_fwd(fake, 8, 16, C.byref(w12), None, 0, fake, 16, None, None) == EINVAL
+    assert L.spmm24_bwd_dx(None, 8, 16, C.byref(w), None, 0, fake, 16, None) == EINVAL
+    assert L.masked_dw_gemm(fake, 16, fake, 16, 8, None, fake, 16, None) == EINVAL
+    # colsum workspace too small
+    assert L.p24_colsum(fake, 100, 16, 16, fake, fake, 8, None) == native.P24_ENOSPACE
+    # ffn step: null args, bad flags, d % 8
+    assert L.ffn24_step(None, fake, 1 << 20, None) == EINVAL
+    a = native.p24_ffn_args(8, 12, 16, 0, fake, fake, None, fake, None, fake, fake, fake, fake, fake, fake,
+                            None, None)
+    assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
+    a.d, a.flags = 16, 0x8
+    assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
+
+
+def test_workspace_sizes_grow_with_the_problem(native):
+    f = native.lib.ffn24_workspace_size
+    assert f(128, 256, 512, 0) < f(256, 256, 512, 0) < f(256, 256, 512, native.P24_STEP_ACT24)
+    assert native.lib.p24_colsum_workspace_size(64, 100) == 400
+    assert native.lib.p24_colsum_workspace_size(10 ** 6, 8) == 1024 * 8 * 4
