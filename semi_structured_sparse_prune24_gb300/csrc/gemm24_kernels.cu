@@ -20,6 +20,13 @@
 // Roles (warp index): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 epilogue
 // (warp w reads TMEM lanes 32*(w%4)..+31), 6-9 (spmm only) metadata movers:
 // smem -> registers -> TMEM, replacing rows past the matrix with a legal pattern.
+//
+// TMEM layout of the sparse metadata read by one tcgen05.mma.sp (kind::f16,
+// M = 128, K = 32): one 32-bit column over the 128 lanes, rows interleaved in
+// blocks of 16. Lane 16b + 8h + i holds, for K-half h (groups 4h..4h+3, 16 bits,
+// group 4h in the low nibble), row 16b + i in bits 0-15 and row 16b + 8 + i in
+// bits 16-31. (Measured on sm_103a with an identity B operand, which makes the
+// accumulator equal to the A operand as the tensor core expanded it.)
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -104,8 +111,8 @@ __device__ __forceinline__ void mask_group(uint32_t& lo, uint32_t& hi, uint32_t 
   hi &= ((kb & 4u) ? 0x0000FFFFu : 0u) | ((kb & 8u) ? 0xFFFF0000u : 0u);
 }
 
-__device__ __forceinline__ void tc_st_32x32b_x2(uint32_t taddr, uint32_t a, uint32_t b) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+__device__ __forceinline__ void tc_st_32x32b_x1(uint32_t taddr, uint32_t a) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -127,14 +134,22 @@ struct SpmmSmem {
   static constexpr int kTx = kA + kB + kE;
 };
 
+// TMEM column of the metadata of MMA j (0/1) of stage s: 8-column slots in the
+// gaps after the two accumulator buffers ([BN, 256) and [256 + BN, 512)).
+template <int BN>
+__device__ __forceinline__ uint32_t meta_col(int s, int j) {
+  constexpr int kGap = (256 - BN) / 8;  // slots per gap
+  const int k = 2 * s + j;
+  return k < kGap ? BN + 8 * k : 256 + BN + 8 * (k - kGap);
+}
+
 template <int BN, int STAGES, bool kTransOut>
 __global__ void __launch_bounds__(320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
   using L = SpmmSmem<BN, STAGES>;
-  constexpr int kAccCols = 256;             // accumulator buffer b starts at column 256 * b
-  constexpr int kMetaCol0 = 256 + BN;       // then 2 metadata columns per stage
-  static_assert(BN <= 256 && 256 + BN + 2 * STAGES <= 512, "TMEM budget");
+  constexpr int kAccCols = 256;  // accumulator buffer b starts at column 256 * b
+  static_assert(BN <= 256 && BN % 8 == 0 && 2 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, /*sparse=*/true, false, false);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -228,7 +243,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int j = 0; j < 2; ++j) {
             const uint64_t adesc = smem_desc(a_base + j * 32, 16, 512, kSwizzle64B);
             const uint64_t bdesc = smem_desc(b_base + j * 64, 16, 1024, kSwizzle128B);
-            tc_mma_sp_f16(d_tmem, adesc, bdesc, tmem + kMetaCol0 + 2 * s + j, kIdesc, (kb | j) != 0);
+            tc_mma_sp_f16(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
           }
           tc_commit(&empty[s]);
         }
@@ -246,22 +261,32 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp >= 6) {
     // ------------------------------------------------ metadata movers
+    // Lane l of quarter q fills TMEM lane 32q + l: rows rA = 32q + (l & 16) + (l & 7)
+    // and rA + 8, K-half h = (l >> 3) & 1 of each MMA's 32 metadata bits.
     const int q = warp & 3;
-    const int row = q * 32 + lane;
+    const int rowA = q * 32 + (lane & 16) + (lane & 7);
+    const int rowB = rowA + 8;
+    const int h = (lane >> 3) & 1;
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
-      const bool row_ok = ta * kBM + row < p.rowsA;
+      const bool okA = ta * kBM + rowA < p.rowsA;
+      const bool okB = ta * kBM + rowB < p.rowsA;
       for (int kb = 0; kb < p.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!p24_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
-        const uint2 e = *reinterpret_cast<const uint2*>(smem + L::kOffE + s * L::kE + row * 16 + (kb & 1) * 8);
-        const uint32_t e0 = row_ok ? e.x : 0x44444444u;
-        const uint32_t e1 = row_ok ? e.y : 0x44444444u;
-        tc_st_32x32b_x2(tmem + (static_cast<uint32_t>(q * 32) << 16) + kMetaCol0 + 2 * s, e0, e1);
+        const uint8_t* e = smem + L::kOffE + s * L::kE + (kb & 1) * 8;
+        const uint2 ea = *reinterpret_cast<const uint2*>(e + rowA * 16);
+        const uint2 eb = *reinterpret_cast<const uint2*>(e + rowB * 16);
+        const uint32_t sh = 16u * h;
+        const uint32_t a0 = okA ? (ea.x >> sh) & 0xFFFFu : 0x4444u, a1 = okA ? (ea.y >> sh) & 0xFFFFu : 0x4444u;
+        const uint32_t b0 = okB ? (eb.x >> sh) & 0xFFFFu : 0x4444u, b1 = okB ? (eb.y >> sh) & 0xFFFFu : 0x4444u;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        tc_st_32x32b_x1(tmem + lane_base + meta_col<BN>(s, 0), a0 | (b0 << 16));
+        tc_st_32x32b_x1(tmem + lane_base + meta_col<BN>(s, 1), a1 | (b1 << 16));
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -584,7 +609,7 @@ int num_sms() {
 }
 
 constexpr int kSpBN = 224;
-constexpr int kSpStages = 5;
+constexpr int kSpStages = 4;
 constexpr int kDwStages = 4;
 
 template <bool kTrans>

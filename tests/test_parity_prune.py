@@ -19,17 +19,21 @@ def P():
 
 
 def make_w(rows, cols, kind, seed=0):
+    """A [rows, cols] bf16 view whose row stride is cols rounded up to 8 (16 bytes)."""
+    ld = (cols + 7) // 8 * 8
     if kind == "normal":
-        return normal_bf16((rows, cols), 1.0, seed, 2, "cuda")
-    if kind == "ints":
-        return small_int_bf16((rows, cols), -2, 2, seed, 2, "cuda")
-    # specials: ints sprinkled with -0, inf, -inf, NaN, subnormals
-    w = bits_of(small_int_bf16((rows, cols), -2, 2, seed, 2))
-    rng = np.random.default_rng(seed)
-    specials = np.array([0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001], np.uint16)
-    pick = rng.random(w.shape) < 0.2
-    w[pick] = specials[rng.integers(0, len(specials), pick.sum())]
-    return from_bits(w, "cuda")
+        w = normal_bf16((rows, ld), 1.0, seed, 2, "cuda")
+    elif kind == "ints":
+        w = small_int_bf16((rows, ld), -2, 2, seed, 2, "cuda")
+    else:
+        # specials: ints sprinkled with -0, inf, -inf, NaN, subnormals
+        b = bits_of(small_int_bf16((rows, ld), -2, 2, seed, 2))
+        rng = np.random.default_rng(seed)
+        specials = np.array([0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001], np.uint16)
+        pick = rng.random(b.shape) < 0.2
+        b[pick] = specials[rng.integers(0, len(specials), pick.sum())]
+        w = from_bits(b, "cuda")
+    return w[:, :cols]
 
 
 SHAPES = [(1, 4), (3, 12), (37, 72), (130, 1028), (257, 1000), (64, 8200)]
@@ -40,7 +44,7 @@ SHAPES = [(1, 4), (3, 12), (37, 72), (130, 1028), (257, 1000), (64, 8200)]
 def test_compress_bit_exact(P, rows, cols, kind):
     W = make_w(rows, cols, kind)
     out = P.Sparse24.empty(rows, cols)
-    Wm = torch.empty_like(W)
+    Wm = torch.empty((rows, (cols + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")[:, :cols]
     P.prune24_compress(W, out, W_masked=Wm)
     gv, gm = sparse_bits(out)
     rv, rm = O.compress24(bits_of(W), out.ldv, out.ldm)
@@ -73,7 +77,8 @@ def test_double_prune_bit_exact(P, rows, cols, kind):
     assert_bits_equal(gv, rv, "bwdT vals")
     assert_bits_equal(gm, rm, "bwdT meta")
     # fused variant: same bits for both outputs
-    f2, b2 = P.prune24_compress_both(W, W_masked=(Wm := torch.empty_like(W)))
+    Wm = torch.empty((rows, (cols + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")[:, :cols]
+    f2, b2 = P.prune24_compress_both(W, W_masked=Wm)
     for a, b, name in ((sparse_bits(f2), (fv, fm), "fwd"), (sparse_bits(b2), (gv, gm), "bwdT")):
         assert_bits_equal(a[0], b[0], f"{name} vals (fused)")
         assert_bits_equal(a[1], b[1], f"{name} meta (fused)")
