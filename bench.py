@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Benchmark: one 2:4 sparse FFN training step (prune both weights fresh,
+forward, double-pruned backward, masked weight gradients) on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. The metric is the step's dense-equivalent
+throughput (12 * M * d * ffn FLOP per step / step time), reported with its
+fraction of the 2:4-sparse bf16 tensor peak; the standalone 1e9-element prune
+is reported beside it in GB/s. Multi-GPU runs are independent replicas (one
+step per GPU, no collective on the data path): weak scaling, value = all
+ranks' FLOP / the slowest rank's time.
+
+--impl reference times the CPU oracle (oracle/, numpy) on the host cores on a
+bounded slice of the same workload; it is a slow reference, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SPARSE_RATIO = 2.0  # nominal 2:4-sparse / dense tensor throughput
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks() -> tuple[dict, str]:
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        ident = str(device_index)
+        try:
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.QUERY}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict | None:
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")  # barrier + timing reduction only
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle (CPU) sample
+def oracle_sample_step(d: int, m_s: int, f_s: int, w_sigma: float, seed: int = 0) -> float:
+    """One oracle step on a slice of the workload: m_s tokens x f_s hidden units
+    (full model width d). Returns seconds. Inputs drawn like the workload's."""
+    import numpy as np  # noqa: F401
+
+    from oracle import prune24_oracle as O
+    from synth24 import normal_bf16
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+    X = bits(normal_bf16((m_s, d), 1.0, seed, 1))
+    Wu = bits(normal_bf16((f_s, d), w_sigma, seed, 2))
+    Wd = bits(normal_bf16((d, f_s), w_sigma, seed, 3))
+    dY = bits(normal_bf16((m_s, d), 1.0, seed, 6))
+    bu = np.zeros(f_s, np.float32)
+    bd = np.zeros(d, np.float32)
+    t0 = time.perf_counter()
+    O.ffn_step(X, Wu, bu, Wd, bd, dY)
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seconds_target: float = 15.0) -> dict:
+    m_s, f_s = 1024, 1024
+    oracle_sample_step(w.d, 64, 64, w.w_sigma)  # import + first-touch warmup
+    times = []
+    t_start = time.perf_counter()
+    while not times or (time.perf_counter() - t_start < seconds_target and len(times) < 20):
+        times.append(oracle_sample_step(w.d, m_s, f_s, w.w_sigma))
+    t = statistics.median(times)
+    flop = 12 * m_s * w.d * f_s
+    return {"value": flop / t / 1e12, "unit": "TFLOPS (dense-equivalent)", "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"oracle ffn_step (numpy fp32 GEMMs via BLAS on all visible cores, prune+double-prune "
+                       f"included) on a slice of the workload: {m_s} tokens x {f_s} hidden units at d={w.d}; "
+                       f"median of {len(times)} runs, {t:.2f} s each")}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import semi_structured_sparse_prune24_gb300 as P
+    from synth24 import WORKLOADS, normal_bf16
+
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+
+    # inputs resident in HBM (seeded per rank)
+    seed = rank
+    X = normal_bf16((w.M, w.d), w.x_sigma, seed, 1, dev)
+    Wu = normal_bf16((w.ffn, w.d), w.w_sigma, seed, 2, dev)
+    Wd = normal_bf16((w.d, w.ffn), w.w_sigma, seed, 3, dev)
+    dY = normal_bf16((w.M, w.d), w.dy_sigma, seed, 6, dev)
+    bu = torch.zeros(w.ffn, dtype=torch.float32, device=dev)
+    bd = torch.zeros(w.d, dtype=torch.float32, device=dev)
+    out = P.ffn24_step(X, Wu, bu, Wd, bd, dY, act24=w.act24)
+    ws = torch.empty(P.ffn24_workspace_size(w.M, w.d, w.ffn, w.act24), dtype=torch.uint8, device=dev)
+
+    def step(events=None):
+        P.ffn24_step(X, Wu, bu, Wd, bd, dY, act24=w.act24, out=out, workspace=ws, events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if P.p24_query_status() != 0:
+        raise RuntimeError("device status word set after warm-up")
+
+    # per-phase events (raw cudaEvent_t handles), created up front
+    nph = P.STEP_PHASES
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nph * args.steps)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    handles = [(ctypes.c_void_p * (2 * nph))(*[evs[i * 2 * nph + j].cuda_event for j in range(2 * nph)])
+               for i in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    launches0 = P.p24_launch_count()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(handles[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = P.p24_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    if P.p24_query_status() != 0:
+        raise RuntimeError("device status word set during the timed steps")
+    ms_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+
+    phase_ms = [statistics.mean(evs[i * 2 * nph + 2 * p].elapsed_time(evs[i * 2 * nph + 2 * p + 1])
+                                for i in range(args.steps)) for p in range(nph)]
+    flop = w.dense_equiv_flop
+    value = world * flop / (ms_step * 1e-3) / 1e12
+    sparse_peak = peaks["bf16_tflops_sustained"] * SPARSE_RATIO
+    dense_peak = peaks["bf16_tflops_sustained"]
+    gemm_flop = 2 * w.M * w.d * w.ffn  # every one of the six GEMMs
+    kernels = {
+        "spmm_kernel (tcgen05.mma.sp)": {"phases": [2, 3, 4, 7], "bound": "tensor", "peak": sparse_peak,
+                                         "per_launch": gemm_flop, "unit": "TFLOP/s"},
+        "dw_kernel (tcgen05.mma, masked)": {"phases": [6, 8], "bound": "tensor", "peak": dense_peak,
+                                            "per_launch": gemm_flop, "unit": "TFLOP/s"},
+        "double_prune_kernel (fused prune + double prune)": {
+            "phases": [0, 1], "bound": "hbm", "peak": peaks["hbm_gbs"],
+            "per_launch": int(4.25 * w.d * w.ffn), "unit": "GB/s"},
+        "colsum (bias gradients)": {"phases": [5], "bound": "hbm", "peak": peaks["hbm_gbs"],
+                                    "per_launch": 2 * w.M * (w.d + w.ffn) // 2, "unit": "GB/s"},
+    }
+    breakdown = {}
+    for name, k in kernels.items():
+        tot = sum(phase_ms[p] for p in k["phases"])
+        avg = tot / len(k["phases"])
+        scale = 1e12 if k["unit"] == "TFLOP/s" else 1e9
+        ach = k["per_launch"] / (avg * 1e-3) / scale
+        breakdown[name] = {"ms_per_step": tot, "launches_per_step": len(k["phases"]), "avg_launch_ms": avg,
+                           "achieved": ach, "unit": k["unit"], "frac": ach / k["peak"]}
+    dominant = max(breakdown, key=lambda n: breakdown[n]["ms_per_step"])
+    dk = kernels[dominant]
+    roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": breakdown[dominant]["achieved"],
+                "peak": dk["peak"], "unit": dk["unit"], "frac": breakdown[dominant]["frac"], "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops_sustained" +
+                               (" x 2 (nominal 2:4 ratio)" if dk["peak"] == sparse_peak else "")
+                               if dk["unit"] == "TFLOP/s" else f"{peak_src} hbm_gbs"}
+
+    # ---- standalone prune of 1e9 bf16 ([31250, 32000]), HBM-bound
+    prune = None
+    if not args.no_prune:
+        del ws
+        torch.cuda.empty_cache()
+        Wp = normal_bf16((31250, 32000), 0.01, seed, 2, dev)
+        sp = P.Sparse24.empty(31250, 32000, dev)
+        for _ in range(args.warmup):
+            P.prune24_compress(Wp, sp)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            P.prune24_compress(Wp, sp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        pms = e0.elapsed_time(e1) / args.steps
+        gbs = 3.125e9 / (pms * 1e-3) / 1e9
+        prune = {"value": gbs, "unit": "GB/s", "ms": pms, "frac_hbm": gbs / peaks["hbm_gbs"],
+                 "elements": 31250 * 32000, "algorithmic_bytes_per_elt": 3.125,
+                 "note": "input 2 GB > L2, no flush needed"}
+        del Wp, sp
+        torch.cuda.empty_cache()
+        ws = torch.empty(P.ffn24_workspace_size(w.M, w.d, w.ffn, w.act24), dtype=torch.uint8, device=dev)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hin = {k: v.cpu().pin_memory() for k, v in (("X", X), ("W_up", Wu), ("W_down", Wd), ("dY", dY))}
+        hout = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory()
+                for k in ("Y", "dX", "dW_up", "dW_down", "db_up", "db_down")}
+        dX_, dWu_, dWd_, ddY_ = (torch.empty_like(t) for t in (X, Wu, Wd, dY))
+        h2d = sum(t.numel() * t.element_size() for t in hin.values())
+        d2h = sum(t.numel() * t.element_size() for t in hout.values())
+
+        def e2e_step():
+            dX_.copy_(hin["X"], non_blocking=True)
+            dWu_.copy_(hin["W_up"], non_blocking=True)
+            dWd_.copy_(hin["W_down"], non_blocking=True)
+            ddY_.copy_(hin["dY"], non_blocking=True)
+            P.ffn24_step(dX_, dWu_, bu, dWd_, bd, ddY_, act24=w.act24, out=out, workspace=ws)
+            for k, t in hout.items():
+                t.copy_(out[k], non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        e2e = {"value": world * flop / (ems * 1e-3) / 1e12, "unit": "TFLOPS (dense-equivalent)", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "pinned host X, dY, W_up, W_down copied in and Y, dX, dW_up, dW_down, db copied out every "
+                       "step, on the step's stream"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": "sparse FFN fwd+bwd dense-equiv TFLOPS, % of 2:4 bf16 TC peak; prune GB/s",
+            "value": value, "unit": "TFLOPS (dense-equivalent)", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "pct_sparse_peak": value / world / sparse_peak,
+            # composite roofline: four sparse GEMMs at the sparse rate, two dW GEMMs at the dense rate
+            "pct_composite_roofline": (4 * gemm_flop / (sparse_peak * 1e12) + 2 * gemm_flop / (dense_peak * 1e12))
+            / (ms_step * 1e-3),
+            "config": {"workload": w.name, "M": w.M, "d": w.d, "ffn": w.ffn, "reprune_every_step": w.reprune,
+                       "act24": w.act24, "global_batch": w.M * world,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"inputs larger than L2 ({L2_BYTES // 2 ** 20} MB): X {X.numel() * 2 >> 20} MB, "
+                             f"W_up/W_down {Wu.numel() * 2 >> 20} MB each; no flush between steps"},
+            "phase_ms": dict(zip(P.STEP_PHASE_NAMES, phase_ms)),
+            "kernels": breakdown,
+            "roofline": roofline,
+            "prune": prune,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "peaks": {"source": peak_src, **peaks, "sparse_ratio": SPARSE_RATIO},
+        }
+        print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+def run_reference(args, world, rank):
+    from synth24 import WORKLOADS
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    m_s, f_s = 512, 512
+    for _ in range(args.warmup):
+        oracle_sample_step(w.d, m_s, f_s, w.w_sigma)
+    times = [oracle_sample_step(w.d, m_s, f_s, w.w_sigma) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    flop = 12 * m_s * w.d * f_s
+    value = flop / t / 1e12
+    sample = (f"oracle ffn_step on a slice of the workload: {m_s} tokens x {f_s} hidden units at d={w.d} "
+              f"(numpy, BLAS on all visible cores)")
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "sparse FFN fwd+bwd dense-equiv TFLOPS, % of 2:4 bf16 TC peak; prune GB/s",
+        "value": value, "unit": "TFLOPS (dense-equivalent)", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 accumulate on bf16 inputs", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "d": w.d, "ffn": w.ffn, "sample_tokens": m_s,
+                   "sample_hidden": f_s},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS (dense-equivalent)", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS (dense-equivalent)", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="70b_m16384")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prune", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -236,6 +236,22 @@ size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags);
 int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * ffn24_step_traced -- ffn24_step that also records caller-created CUDA events
+ * (cudaEvent_t handles) on `stream` around each phase of the step, for
+ * per-kernel timing without a synchronisation: events[2p] before and
+ * events[2p+1] after phase p, for p < min(P24_STEP_PHASES, n_events / 2).
+ * Phases: 0 prune+double-prune W_up, 1 the same for W_down, 2 up forward (H),
+ * 3 down forward (Y), 4 down backward dX (dH), 5 bias gradients, 6 dW_down,
+ * 7 up backward dX, 8 dW_up. events may be NULL (then identical to ffn24_step).
+ */
+#define P24_STEP_PHASES 9
+int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream,
+                      void* const* events, int n_events);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t p24_launch_count(void);
+
+/*
  * p24_query_status -- synchronise `stream`, then return and clear the device
  * status word of the current GPU: P24_OK, or P24_ETIMEOUT if a kernel gave up
  * a bounded wait (the kernel then skipped its remaining work and exited

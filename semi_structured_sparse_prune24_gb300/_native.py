@@ -61,6 +61,8 @@ def _load() -> C.CDLL:
         "p24_colsum": (i32, [vp, i64, i64, i64, vp, vp, sz, vp]),
         "ffn24_workspace_size": (sz, [i64, i64, i64, u32]),
         "ffn24_step": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp]),
+        "ffn24_step_traced": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp, C.POINTER(vp), i32]),
+        "p24_launch_count": (C.c_uint64, []),
         "p24_query_status": (i32, [vp]),
         "p24_strerror": (C.c_char_p, [i32]),
     }
@@ -258,9 +260,17 @@ def ffn24_workspace_size(M: int, d: int, ffn: int, act24: bool = False) -> int:
     return int(lib.ffn24_workspace_size(M, d, ffn, P24_STEP_ACT24 if act24 else 0))
 
 
+STEP_PHASES = 9
+STEP_PHASE_NAMES = ("prune_up", "prune_down", "up_fwd", "down_fwd", "down_bwd_dx", "bias_grads", "dW_down",
+                    "up_bwd_dx", "dW_up")
+
+
 def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict | None = None,
-               workspace: torch.Tensor | None = None, stream=None) -> dict:
-    """One 2:4 FFN layer fwd+bwd; returns dict(Y, H, dX, dW_up, dW_down, db_up, db_down)."""
+               workspace: torch.Tensor | None = None, stream=None, events=None) -> dict:
+    """One 2:4 FFN layer fwd+bwd; returns dict(Y, H, dX, dW_up, dW_down, db_up, db_down).
+
+    events: optional ctypes array of 2 * STEP_PHASES raw cudaEvent_t handles, recorded
+    before/after each phase (see ffn24_step_traced in include/prune24.h)."""
     M, d, _ = _mat(X, name="X")
     ffn = W_up.shape[0]
     dev = X.device
@@ -284,8 +294,16 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
                      W_down.data_ptr(), _ptr(b_down), dY.data_ptr(), o["Y"].data_ptr(), o["H"].data_ptr(),
                      o["dX"].data_ptr(), o["dW_up"].data_ptr(), o["dW_down"].data_ptr(), _ptr(o["db_up"]),
                      _ptr(o["db_down"]))
-    _check(lib.ffn24_step(C.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "ffn24_step")
+    if events is None:
+        _check(lib.ffn24_step(C.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "ffn24_step")
+    else:
+        _check(lib.ffn24_step_traced(C.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream),
+                                     C.cast(events, C.POINTER(C.c_void_p)), len(events)), "ffn24_step_traced")
     return o
+
+
+def p24_launch_count() -> int:
+    return int(lib.p24_launch_count())
 
 
 def p24_query_status(stream=None) -> int:

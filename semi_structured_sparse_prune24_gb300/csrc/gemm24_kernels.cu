@@ -622,6 +622,7 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   if (err != cudaSuccess) return err;
   const int grid = std::min(p.num_tiles, num_sms());
   kern<<<grid, 320, smem, s>>>(a, b, e, p);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -697,6 +698,7 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
   if (err != cudaSuccess) return err;
   const int grid = std::min(p.num_tiles, num_sms());
   kern<<<grid, 192, smem, s>>>(ta, tb, p);
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 // workspace carving for the FFN step, and the device status word.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -90,6 +91,9 @@ void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, char* base, 
 }
 
 }  // namespace
+
+std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int* device_status_ptr() {
   int* p = nullptr;
@@ -241,7 +245,15 @@ size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags) {
 }
 
 int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream) {
+  return ffn24_step_traced(a, workspace, ws_bytes, stream, nullptr, 0);
+}
+
+uint64_t p24_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream, void* const* events,
+                      int n_events) {
   if (!a) return P24_EINVAL;
+  if (n_events < 0 || (n_events > 0 && !events)) return P24_EINVAL;
   if (a->flags & ~P24_STEP_ACT24) return P24_EINVAL;
   const int64_t M = a->M, d = a->d, ffn = a->ffn;
   if (M < 0 || d <= 0 || ffn <= 0 || d % 8 != 0 || ffn % 8 != 0) return P24_EINVAL;
@@ -270,10 +282,21 @@ int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* st
   const cudaStream_t s = as_stream(stream);
   int* st = device_status_ptr();
   if (!st) return P24_ECUDA;
+  const int n_ph = n_events / 2 < P24_STEP_PHASES ? n_events / 2 : P24_STEP_PHASES;
+  auto mark = [&](int phase, int edge) -> int {
+    if (phase >= n_ph) return P24_OK;
+    return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(events[2 * phase + edge]), s));
+  };
+#define P24_PHASE(ph, body)   \
+  do {                        \
+    P24_TRY(mark(ph, 0));     \
+    body;                     \
+    P24_TRY(mark(ph, 1));     \
+  } while (0)
 
   // 1. fresh 2:4 masks of both weights, and their double-pruned transposes
-  P24_TRY(cuda_status(launch_compress_both(a->W_up, ffn, d, d, L.up_fwd, L.up_bwdT, nullptr, 0, s)));
-  P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT, wdm, ffn, s)));
+  P24_PHASE(0, P24_TRY(cuda_status(launch_compress_both(a->W_up, ffn, d, d, L.up_fwd, L.up_bwdT, nullptr, 0, s))));
+  P24_PHASE(1, P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT, wdm, ffn, s))));
   if (M == 0) {
     if (a->db_up) P24_TRY(cuda_status(cudaMemsetAsync(a->db_up, 0, ffn * 4, s)));
     if (a->db_down) P24_TRY(cuda_status(cudaMemsetAsync(a->db_down, 0, d * 4, s)));
@@ -285,32 +308,38 @@ int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* st
   up.bias = a->b_up;
   up.relu = true;
   if (act24) up.act24 = L.hs;
-  P24_TRY(cuda_status(launch_spmm(L.up_fwd, a->X, M, d, a->H, ffn, true, up, st, s)));
-  if (act24) P24_TRY(cuda_status(launch_pad(L.hs, s)));
+  P24_PHASE(2, {
+    P24_TRY(cuda_status(launch_spmm(L.up_fwd, a->X, M, d, a->H, ffn, true, up, st, s)));
+    if (act24) P24_TRY(cuda_status(launch_pad(L.hs, s)));
+  });
   // 3. Y = H W_down^T + b_down
   EpiArgs dn;
   dn.bias = a->b_down;
   if (act24)
-    P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s)));
+    P24_PHASE(3, P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s))));
   else
-    P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s)));
+    P24_PHASE(3, P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s))));
   // 4. dH = (dY W_down_bwd) * [H > 0]
   EpiArgs g;
   g.gate = a->H;
   g.ldg = ffn;
-  P24_TRY(cuda_status(launch_spmm(L.dn_bwdT, a->dY, M, d, dHv, ffn, true, g, st, s)));
+  P24_PHASE(4, P24_TRY(cuda_status(launch_spmm(L.dn_bwdT, a->dY, M, d, dHv, ffn, true, g, st, s))));
   // 5. bias gradients
-  if (a->db_up) P24_TRY(cuda_status(launch_colsum(dHv, M, ffn, ffn, a->db_up, cs, s)));
-  if (a->db_down) P24_TRY(cuda_status(launch_colsum(a->dY, M, d, d, a->db_down, cs, s)));
+  P24_PHASE(5, {
+    if (a->db_up) P24_TRY(cuda_status(launch_colsum(dHv, M, ffn, ffn, a->db_up, cs, s)));
+    if (a->db_down) P24_TRY(cuda_status(launch_colsum(a->dY, M, d, d, a->db_down, cs, s)));
+  });
   // 6. dW_down = (dY^T H) on mask(W_down)
-  P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm, a->dW_down,
-                                       ffn, st, s)));
+  P24_PHASE(6, P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm,
+                                                    a->dW_down, ffn, st, s))));
   // 7. dX = dH W_up_bwd
   EpiArgs none;
-  P24_TRY(cuda_status(launch_spmm(L.up_bwdT, dHv, M, ffn, a->dX, d, true, none, st, s)));
+  P24_PHASE(7, P24_TRY(cuda_status(launch_spmm(L.up_bwdT, dHv, M, ffn, a->dX, d, true, none, st, s))));
   // 8. dW_up = (dH^T X) on mask(W_up)
-  return cuda_status(
-      launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s));
+  P24_PHASE(8, P24_TRY(cuda_status(
+                   launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s))));
+#undef P24_PHASE
+  return P24_OK;
 }
 
 int p24_query_status(void* stream) {

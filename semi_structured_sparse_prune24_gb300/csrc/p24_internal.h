@@ -40,4 +40,7 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
 
 int* device_status_ptr();  // the status word of the current device
 
+// Count one kernel launch (called by every launcher after a successful launch).
+void count_launch();
+
 }  // namespace p24

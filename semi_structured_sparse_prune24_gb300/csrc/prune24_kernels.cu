@@ -286,6 +286,7 @@ cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 16);
   pad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<uint16_t*>(d.vals), d.ldv, d.meta, d.ldm,
                                                            d.rows, d.cols);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -301,6 +302,7 @@ cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t l
                                                static_cast<uint16_t*>(W_masked), ldwm);
   else
     compress_kernel<false><<<grid, 256, 0, s>>>(w, rows, cols, ldw, v, out.ldv, out.meta, out.ldm, nullptr, 0);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_pad(out, s);
@@ -321,6 +323,7 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
     double_prune_kernel<true, false><<<grid, 256, 0, s>>>(
         w, ldw, nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm, rows, cols,
         static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = launch_pad(fwd, s)) != cudaSuccess) return e;
@@ -336,6 +339,7 @@ cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwd
   double_prune_kernel<false, false><<<grid, 256, 0, s>>>(
       nullptr, 0, static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm, rows, cols,
       static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_pad(bwdT, s);
@@ -355,9 +359,11 @@ cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, floa
   const int64_t rps = (M + S - 1) / S;
   dim3 grid(static_cast<unsigned>((N + 511) / 512), static_cast<unsigned>(S));
   colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), M, N, ldg, rps, ws);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   colsum_final_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(ws, S, N, out);
+  count_launch();
   return cudaGetLastError();
 }
 
