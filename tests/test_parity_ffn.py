@@ -3,9 +3,11 @@
 The oracle runs independently on the same seeded inputs. Two decisions in the
 step are taken on rounded values (the ReLU gate on bf16 H, and with 2:4
 activations the activation pick on bf16 H); where the GPU's and the oracle's
-fp32 sums differ by rounding, such a decision can legitimately differ. Those
-positions are validated as near-ties and excluded from the elementwise check
-of the tensors they directly select; every other output is compared in full.
+fp32 sums differ by rounding (a pre-activation within rounding of 0, two
+magnitudes within rounding of each other), either decision is correct. Such
+positions are located, validated as near-zero / near-tie, and only the token
+rows and hidden units they select are left out of the elementwise check; the
+normwise check covers every output in full.
 """
 import numpy as np
 import pytest
@@ -32,38 +34,63 @@ def run_gpu(P, inp, act24):
     return o
 
 
-def act_flip_rows(Hg_bits, ref, ffn):
-    """Rows whose GPU activation mask differs from the oracle's; each flip must be a near-tie."""
+def act_flip_groups(Hg_bits, ref, ffn):
+    """[M, ffn/4] bool: activation groups whose GPU 2:4 pick differs from the oracle's.
+    Each must be a near-tie: the two picks keep magnitudes equal up to bf16 rounding."""
     mg = O.mask_from_meta(O.compress24(Hg_bits)[1], ffn)
     mr = O.mask_from_meta(ref["Hs_meta"], ffn)
-    diff = (mg != mr).reshape(mg.shape[0], -1, 4).any(-1)          # [M, groups]
-    rows = np.unique(np.nonzero(diff)[0])
+    diff = (mg != mr).reshape(mg.shape[0], -1, 4).any(-1)
     for m, g in zip(*np.nonzero(diff)):
         h = np.abs(ref["H_ref"][m, 4 * g:4 * g + 4])
         kept_r = h[mr[m, 4 * g:4 * g + 4]]
         kept_g = h[mg[m, 4 * g:4 * g + 4]]
-        # the two picks keep magnitudes equal up to bf16 rounding
         assert np.allclose(np.sort(kept_r), np.sort(kept_g), rtol=2 ** -7, atol=1e-6), (m, g, h)
-    return rows
+    return diff
+
+
+def disputed_positions(o, ref, w: FFNWorkload, act24: bool):
+    """Token rows and hidden units touched by a decision taken on rounded values
+    that the GPU and the oracle legitimately took differently:
+      - ReLU gate [H > 0] where the pre-activation is within rounding of 0
+        (the positive side's value must be tiny), and
+      - with 2:4 activations, groups whose pick is a near-tie.
+    Returns (rows m, hidden units f, count)."""
+    Hg = O.bf16_to_f32(bits_of(o["H"]))
+    Hr = O.bf16_to_f32(ref["H_used"])
+    disputed = np.zeros(Hg.shape, dtype=bool)
+    if act24:
+        groups = act_flip_groups(bits_of(o["H"]), ref, w.ffn)
+        disputed |= np.repeat(groups, 4, axis=1)
+    gate = ((Hg > 0) != (Hr > 0)) & ~disputed
+    scale = float(np.sqrt(np.mean(ref["H_ref"].astype(np.float64) ** 2))) or 1.0
+    near_zero = np.maximum(Hg, Hr)[gate]
+    assert np.all(near_zero <= 1e-3 * scale), (near_zero.max(), scale)
+    disputed |= gate
+    n = int(disputed.sum())
+    assert n <= 16 + 1e-5 * disputed.size, n
+    ms, fs = np.nonzero(disputed)
+    return np.unique(ms), np.unique(fs), n
 
 
 def compare_step(o, ref, w: FFNWorkload, act24: bool):
-    if act24:
-        Hg = bits_of(o["H"])
-        rows = act_flip_rows(Hg, ref, w.ffn)
-        assert len(rows) <= max(2, w.M // 100), len(rows)
-        keep = np.setdiff1d(np.arange(w.M), rows)
-        Hm = O.bf16_to_f32(ref["H_used"])
-        assert_close(o["H"][torch.as_tensor(keep, device="cuda")], Hm[keep], "H (rows without a near-tie)")
-        assert_close(o["Y"][torch.as_tensor(keep, device="cuda")], ref["Y_ref"][keep], "Y (rows without a near-tie)")
-    else:
-        assert_close(o["H"], ref["H_ref"], "H")
-        assert_close(o["Y"], ref["Y_ref"], "Y")
-    assert_close(o["dX"], ref["dX_ref"], "dX")
-    assert_close(o["dW_up"], ref["dW_up_ref"], "dW_up")
-    assert_close(o["dW_down"], ref["dW_down_ref"], "dW_down")
-    assert_close(o["db_up"], ref["db_up"], "db_up")
+    """Normwise on every output; elementwise everywhere except the rows/units a
+    disputed rounded decision selects (see disputed_positions)."""
+    ms, fs, _ = disputed_positions(o, ref, w, act24)
+    km = np.setdiff1d(np.arange(w.M), ms)
+    kf = np.setdiff1d(np.arange(w.ffn), fs)
+    tm = lambda a: torch.as_tensor(a, device="cuda")  # noqa: E731
+    Hm = O.bf16_to_f32(ref["H_used"]) if act24 else ref["H_ref"]
+    assert_close(o["H"][tm(km)], Hm[km], "H")
+    assert_close(o["Y"][tm(km)], ref["Y_ref"][km], "Y")
+    assert_close(o["dX"][tm(km)], ref["dX_ref"][km], "dX")
+    assert_close(o["dW_up"][tm(kf)], ref["dW_up_ref"][kf], "dW_up")
+    assert_close(o["db_up"][tm(kf)], ref["db_up"][kf], "db_up")
+    assert_close(o["dW_down"][:, tm(kf)], ref["dW_down_ref"][:, kf], "dW_down")
     assert_close(o["db_down"], ref["db_down"], "db_down")
+    for key in ("Y", "dX", "dW_up", "dW_down"):       # normwise over everything
+        g = o[key].float().cpu().numpy().astype(np.float64)
+        r = ref[key + "_ref"].astype(np.float64)
+        assert np.linalg.norm(g - r) <= 5e-3 * np.linalg.norm(r), key
     # masked gradients are exactly zero off the forward masks
     assert np.all(bits_of(o["dW_up"])[~O.mask_from_meta(ref["up_meta"], w.d)] == 0)
     assert np.all(bits_of(o["dW_down"])[~O.mask_from_meta(ref["down_meta"], w.ffn)] == 0)
@@ -108,6 +135,15 @@ def test_ffn_step_70b_bench_workload_sampled(P):
     fs = np.sort(rng.choice(w.ffn, 16, replace=False))
     ns = np.sort(rng.choice(w.d, 16, replace=False))
     tm = lambda a: torch.as_tensor(a, device="cuda")  # noqa: E731
+    def gate_flips(H_gpu, H_bits, H_ref):
+        """ReLU-gate decisions taken differently on the two sides; each must sit at a
+        pre-activation within rounding of 0 (see the module docstring)."""
+        g, r = O.bf16_to_f32(bits_of(H_gpu)), O.bf16_to_f32(H_bits)
+        flip = (g > 0) != (r > 0)
+        scale = float(np.sqrt(np.mean(H_ref.astype(np.float64) ** 2))) or 1.0
+        assert np.all(np.maximum(g, r)[flip] <= 1e-3 * scale)
+        return flip
+
     # token rows: H, Y, dX
     H_r, H_b = O.spmm24_fwd(X[ms], up_v, up_m, w.d, relu=True)
     assert_close(o["H"][tm(ms)], H_r, "H rows")
@@ -115,13 +151,17 @@ def test_ffn_step_70b_bench_workload_sampled(P):
     assert_close(o["Y"][tm(ms)], Y_r, "Y rows")
     _, dH_b = O.spmm24_bwd_dx(dY[ms], dnT_v, dnT_m, w.d, gate=H_b)
     dX_r, _ = O.spmm24_bwd_dx(dH_b, upT_v, upT_m, w.ffn)
-    assert_close(o["dX"][tm(ms)], dX_r, "dX rows")
+    keep = ~gate_flips(o["H"][tm(ms)], H_b, H_r).any(axis=1)
+    assert keep.sum() >= len(ms) - 2
+    assert_close(o["dX"][tm(ms[keep])], dX_r[keep], "dX rows")
     # weight rows: dW_up[fs, :] needs dH[:, fs] over all tokens
-    _, Hc_b = O.spmm24_fwd(X, up_v[fs], up_m[fs], w.d, relu=True)           # H[:, fs]
+    Hc_r, Hc_b = O.spmm24_fwd(X, up_v[fs], up_m[fs], w.d, relu=True)        # H[:, fs]
     _, dHc_b = O.spmm24_bwd_dx(dY, dnT_v[fs], dnT_m[fs], w.d, gate=Hc_b)     # dH[:, fs]
     dWu_r, _ = O.masked_dw(dHc_b, X, up_m[fs])
-    assert_close(o["dW_up"][tm(fs)], dWu_r, "dW_up rows")
-    assert_close(o["db_up"][tm(fs)], O.colsum(dHc_b), "db_up entries")
+    keep = ~gate_flips(o["H"][:, tm(fs)], Hc_b, Hc_r).any(axis=0)
+    assert keep.sum() >= len(fs) - 2
+    assert_close(o["dW_up"][tm(fs[keep])], dWu_r[keep], "dW_up rows")
+    assert_close(o["db_up"][tm(fs[keep])], O.colsum(dHc_b)[keep], "db_up entries")
     # dW_down[ns, :] = dY[:, ns]^T H on the mask: needs the oracle's whole H
     _, H_all = O.spmm24_fwd(X, up_v, up_m, w.d, relu=True)
     dWd_r, _ = O.masked_dw(dY[:, ns], H_all, dn_m[ns])
