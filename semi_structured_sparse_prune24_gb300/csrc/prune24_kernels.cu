@@ -120,106 +120,126 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
 }
 
 // ---------------------------------------------------------------- double prune
-// One warp = one 32-column chunk of a 128-row block; lane l owns the row quad
-// 4h..4h+3 (h = block*32 + l). It holds the quad's 4 x 32 forward-masked values
-// in registers, so each of the 32 column groups (4 rows, one column) is pruned
-// without shared memory, and lanes write consecutive groups of a W_bwd^T row.
-// kFromDense: the input is the dense W (the forward prune happens here too);
-// otherwise the input is the compressed forward matrix.
+// A CTA owns a 128-row x 128-column tile of W_fwd. Load phase: coalesced 16-byte
+// pieces (thread = row piece), the forward prune of dense input happens here and
+// the forward outputs are written straight out; the forward-masked tile goes to
+// shared memory with its 16-byte chunks XOR-swizzled by the row quad, so that in
+// the column phase a warp (lane = row quad) reads 4 rows x 16 bytes per lane
+// without bank conflicts. Column phase: each lane prunes the 4-row column groups
+// of its quad and lanes write consecutive groups of a W_bwd^T row (coalesced).
+// kFromDense: input is the dense W; otherwise the compressed forward matrix.
+constexpr int kDpRows = 128, kDpCols = 128, kDpChunks = kDpCols / 8;
+
 template <bool kFromDense, bool kMasked>
-__global__ void __launch_bounds__(256) double_prune_kernel(
-    const uint16_t* __restrict__ W, int64_t ldw,                       // dense input (kFromDense)
+__global__ void __launch_bounds__(256, 2) double_prune_kernel(
+    const uint16_t* __restrict__ W, int64_t ldw,                        // dense input (kFromDense)
     const uint16_t* __restrict__ fv_in, uint16_t* __restrict__ fv_out,  // forward vals (in / out)
     int64_t ldfv,
-    const uint8_t* __restrict__ fm_in, uint8_t* __restrict__ fm_out,   // forward meta (in / out)
+    const uint8_t* __restrict__ fm_in, uint8_t* __restrict__ fm_out,    // forward meta (in / out)
     int64_t ldfm, int64_t rows, int64_t cols,
     uint16_t* __restrict__ tv, int64_t ldtv, uint8_t* __restrict__ tm, int64_t ldtm,
     uint16_t* __restrict__ Wm, int64_t ldwm) {
-  const int lane = threadIdx.x & 31;
-  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int64_t c0 = chunk * 32;
-  if (c0 >= cols) return;  // uniform per warp
+  __shared__ uint4 tile[kDpRows * kDpChunks];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kDpCols;
   const int64_t nquads = rows / 4;
-  const int64_t ngroups_t = nquads;  // groups per W_bwd^T row
+  const int c = threadIdx.x & (kDpChunks - 1);  // load phase: chunk of the thread
+  const int rb = threadIdx.x >> 4;               // load phase: first row of the thread
 
-  for (int64_t qb = blockIdx.y; qb * 32 < nquads; qb += gridDim.y) {
-    const int64_t h = qb * 32 + lane;
-    const bool active = h < nquads;
-    uint32_t d[4][16];  // [row of quad][word]: word w holds columns c0+2w, c0+2w+1
+  for (int64_t row0 = static_cast<int64_t>(blockIdx.y) * kDpRows; row0 < rows;
+       row0 += static_cast<int64_t>(gridDim.y) * kDpRows) {
+    // ---------------- load (+ forward prune)
+    uint4 v[8];
+    const int64_t e = col0 + 8 * c;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int64_t row = 4 * h + r;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {  // 8-column pieces
-        const int64_t e = c0 + 8 * p;
-        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-        const bool full = active && e + 8 <= cols;
-        const bool half = active && !full && e + 4 <= cols;
-        if (kFromDense) {
-          if (full) {
-            const uint4 x = ld_stream_v4(W + row * ldw + e);
-            w0 = x.x; w1 = x.y; w2 = x.z; w3 = x.w;
-          } else if (half) {
-            const uint2 x = __ldcs(reinterpret_cast<const uint2*>(W + row * ldw + e));
-            w0 = x.x; w1 = x.y;
-          }
-          if (full || half) {
-            const uint32_t n0 = pick2_nibble(w0, w1);
-            const uint32_t k0 = kept_pair(w0, w1, n0);
-            uint32_t n1 = 0x4u, k1 = 0;
-            if (full) {
-              n1 = pick2_nibble(w2, w3);
-              k1 = kept_pair(w2, w3, n1);
-            }
-            masked_group(w0, w1, n0, w0, w1);
-            if (full) masked_group(w2, w3, n1, w2, w3);
-            uint16_t* vout = fv_out + row * ldfv + e / 2;
-            if (full) *reinterpret_cast<uint2*>(vout) = make_uint2(k0, k1);
-            else *reinterpret_cast<uint32_t*>(vout) = k0;
-            fm_out[row * ldfm + e / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
-            if (kMasked) {
-              if (full) *reinterpret_cast<uint4*>(Wm + row * ldwm + e) = make_uint4(w0, w1, w2, w3);
-              else *reinterpret_cast<uint2*>(Wm + row * ldwm + e) = make_uint2(w0, w1);
-            }
-          }
+    for (int i = 0; i < 8; ++i) {
+      const int64_t row = row0 + rb + 16 * i;
+      v[i] = make_uint4(0, 0, 0, 0);
+      const bool full = row < rows && e + 8 <= cols;
+      const bool half = row < rows && !full && e + 4 <= cols;
+      if (kFromDense) {
+        if (full) v[i] = ld_stream_v4(W + row * ldw + e);
+        else if (half) {
+          const uint2 x = __ldcs(reinterpret_cast<const uint2*>(W + row * ldw + e));
+          v[i].x = x.x;
+          v[i].y = x.y;
+        }
+      } else if (full || half) {
+        const uint32_t mb = fm_in[row * ldfm + e / 8];
+        if (full) {
+          const uint2 pr = *reinterpret_cast<const uint2*>(fv_in + row * ldfv + e / 2);
+          expand_group(pr.x, mb & 0xFu, v[i].x, v[i].y);
+          expand_group(pr.y, mb >> 4, v[i].z, v[i].w);
         } else {
-          if (full || half) {
-            const uint32_t mb = fm_in[row * ldfm + e / 8];
-            if (full) {
-              const uint2 pr = *reinterpret_cast<const uint2*>(fv_in + row * ldfv + e / 2);
-              expand_group(pr.x, mb & 0xFu, w0, w1);
-              expand_group(pr.y, mb >> 4, w2, w3);
-            } else {
-              const uint32_t pr = *reinterpret_cast<const uint32_t*>(fv_in + row * ldfv + e / 2);
-              expand_group(pr, mb & 0xFu, w0, w1);
-            }
+          const uint32_t pr = *reinterpret_cast<const uint32_t*>(fv_in + row * ldfv + e / 2);
+          expand_group(pr, mb & 0xFu, v[i].x, v[i].y);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = rb + 16 * i;
+      const int64_t row = row0 + r;
+      if (kFromDense) {
+        const bool full = row < rows && e + 8 <= cols;
+        const bool half = row < rows && !full && e + 4 <= cols;
+        if (full || half) {
+          const uint32_t n0 = pick2_nibble(v[i].x, v[i].y);
+          const uint32_t k0 = kept_pair(v[i].x, v[i].y, n0);
+          masked_group(v[i].x, v[i].y, n0, v[i].x, v[i].y);
+          if (full) {
+            const uint32_t n1 = pick2_nibble(v[i].z, v[i].w);
+            const uint32_t k1 = kept_pair(v[i].z, v[i].w, n1);
+            masked_group(v[i].z, v[i].w, n1, v[i].z, v[i].w);
+            *reinterpret_cast<uint2*>(fv_out + row * ldfv + e / 2) = make_uint2(k0, k1);
+            fm_out[row * ldfm + e / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
+            if (kMasked) *reinterpret_cast<uint4*>(Wm + row * ldwm + e) = v[i];
+          } else {
+            *reinterpret_cast<uint32_t*>(fv_out + row * ldfv + e / 2) = k0;
+            fm_out[row * ldfm + e / 8] = static_cast<uint8_t>(n0 | 0x40u);
+            if (kMasked) *reinterpret_cast<uint2*>(Wm + row * ldwm + e) = make_uint2(v[i].x, v[i].y);
           }
         }
-        d[r][4 * p + 0] = w0;
-        d[r][4 * p + 1] = w1;
-        d[r][4 * p + 2] = w2;
-        d[r][4 * p + 3] = w3;
       }
+      tile[r * kDpChunks + (c ^ ((r >> 2) & (kDpChunks - 1)))] = v[i];
     }
-    // Column groups: column c0+k, rows 4h..4h+3.
+    __syncthreads();
+
+    // ---------------- column groups: lane = row quad, warp = 2 chunks (16 columns)
+    const int h = lane;
+    const int64_t hq = row0 / 4 + h;  // global quad = group index along W_bwd^T rows
+    const bool active = hq < nquads;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int64_t col = c0 + k;
-      if (col >= cols) break;  // uniform per warp
-      const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
-      const uint32_t lo = __byte_perm(d[0][k >> 1], d[1][k >> 1], sel);
-      const uint32_t hi = __byte_perm(d[2][k >> 1], d[3][k >> 1], sel);
-      const uint32_t nib = pick2_nibble(lo, hi);
-      const uint32_t pair = kept_pair(lo, hi, nib);
-      const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
-      if (active) {
-        *reinterpret_cast<uint32_t*>(tv + col * ldtv + 2 * h) = pair;
-        if ((lane & 1) == 0) {
-          const uint32_t hiNib = (h + 1 < ngroups_t) ? nib_next : 0x4u;
-          tm[col * ldtm + h / 2] = static_cast<uint8_t>(nib | (hiNib << 4));
+    for (int cc = 0; cc < 2; ++cc) {
+      const int chunk = 2 * warp + cc;
+      if (col0 + 8 * chunk >= cols) break;  // uniform per warp
+      uint4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = tile[(4 * h + i) * kDpChunks + (chunk ^ (h & (kDpChunks - 1)))];
+      const uint32_t w0[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+      const uint32_t w1[4] = {q[1].x, q[1].y, q[1].z, q[1].w};
+      const uint32_t w2[4] = {q[2].x, q[2].y, q[2].z, q[2].w};
+      const uint32_t w3[4] = {q[3].x, q[3].y, q[3].z, q[3].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t col = col0 + 8 * chunk + j;
+        if (col >= cols) break;  // uniform per warp
+        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+        const uint32_t lo = __byte_perm(w0[j >> 1], w1[j >> 1], sel);
+        const uint32_t hi = __byte_perm(w2[j >> 1], w3[j >> 1], sel);
+        const uint32_t nib = pick2_nibble(lo, hi);
+        const uint32_t pair = kept_pair(lo, hi, nib);
+        const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
+        if (active) {
+          *reinterpret_cast<uint32_t*>(tv + col * ldtv + 2 * hq) = pair;
+          if ((lane & 1) == 0) {
+            const uint32_t hi_nib = (hq + 1 < nquads) ? nib_next : 0x4u;
+            tm[col * ldtm + hq / 2] = static_cast<uint8_t>(nib | (hi_nib << 4));
+          }
         }
       }
     }
+    __syncthreads();
   }
 }
 
@@ -311,9 +331,7 @@ cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t l
 cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& fwd,
                                  const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  const int64_t chunks = (cols + 31) / 32;
-  const int64_t qblocks = (rows / 4 + 31) / 32;
-  dim3 grid(static_cast<unsigned>((chunks + 7) / 8), grid_y(qblocks));
+  dim3 grid(static_cast<unsigned>((cols + kDpCols - 1) / kDpCols), grid_y((rows + kDpRows - 1) / kDpRows));
   const auto* w = static_cast<const uint16_t*>(W);
   if (W_masked)
     double_prune_kernel<true, true><<<grid, 256, 0, s>>>(
@@ -333,9 +351,7 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
 cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s) {
   const int64_t rows = fwd.rows, cols = fwd.cols;
   if (rows == 0 || cols == 0) return cudaSuccess;
-  const int64_t chunks = (cols + 31) / 32;
-  const int64_t qblocks = (rows / 4 + 31) / 32;
-  dim3 grid(static_cast<unsigned>((chunks + 7) / 8), grid_y(qblocks));
+  dim3 grid(static_cast<unsigned>((cols + kDpCols - 1) / kDpCols), grid_y((rows + kDpRows - 1) / kDpRows));
   double_prune_kernel<false, false><<<grid, 256, 0, s>>>(
       nullptr, 0, static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm, rows, cols,
       static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);

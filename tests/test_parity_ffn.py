@@ -16,7 +16,7 @@ import torch
 from oracle import prune24_oracle as O
 from synth24 import WORKLOADS, FFNWorkload, ffn_inputs
 from tests.conftest import bits_of
-from tests.p24_testutil import assert_close
+from tests.p24_testutil import assert_close, propagated, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -74,18 +74,26 @@ def disputed_positions(o, ref, w: FFNWorkload, act24: bool):
 
 def compare_step(o, ref, w: FFNWorkload, act24: bool):
     """Normwise on every output; elementwise everywhere except the rows/units a
-    disputed rounded decision selects (see disputed_positions)."""
+    disputed rounded decision selects (see disputed_positions). Outputs computed
+    from a bf16 intermediate (H or dH) get the propagated-rounding term on top of
+    the elementwise bound: the two sides round that intermediate independently."""
     ms, fs, _ = disputed_positions(o, ref, w, act24)
     km = np.setdiff1d(np.arange(w.M), ms)
     kf = np.setdiff1d(np.arange(w.ffn), fs)
     tm = lambda a: torch.as_tensor(a, device="cuda")  # noqa: E731
+    uH2 = ulp_bf16(ref["H_used"]) ** 2                                   # [M, ffn]
+    udH2 = ulp_bf16(ref["dH"]) ** 2                                      # [M, ffn]
+    Wd2 = O.bf16_to_f32(O.decompress24(ref["down_vals"], ref["down_meta"], w.ffn)) ** 2      # [d, ffn]
+    WubT2 = O.bf16_to_f32(O.decompress24(ref["upT_vals"], ref["upT_meta"], w.ffn)) ** 2      # [d, ffn]
+    X2 = O.bf16_to_f32(ref["X"]) ** 2
+    dY2 = O.bf16_to_f32(ref["dY"]) ** 2
     Hm = O.bf16_to_f32(ref["H_used"]) if act24 else ref["H_ref"]
     assert_close(o["H"][tm(km)], Hm[km], "H")
-    assert_close(o["Y"][tm(km)], ref["Y_ref"][km], "Y")
-    assert_close(o["dX"][tm(km)], ref["dX_ref"][km], "dX")
-    assert_close(o["dW_up"][tm(kf)], ref["dW_up_ref"][kf], "dW_up")
-    assert_close(o["db_up"][tm(kf)], ref["db_up"][kf], "db_up")
-    assert_close(o["dW_down"][:, tm(kf)], ref["dW_down_ref"][:, kf], "dW_down")
+    assert_close(o["Y"][tm(km)], ref["Y_ref"][km], "Y", propagated(uH2[km], Wd2.T))
+    assert_close(o["dX"][tm(km)], ref["dX_ref"][km], "dX", propagated(udH2[km], WubT2.T))
+    assert_close(o["dW_up"][tm(kf)], ref["dW_up_ref"][kf], "dW_up", propagated(udH2[:, kf].T, X2))
+    assert_close(o["db_up"][tm(kf)], ref["db_up"][kf], "db_up", 4 * np.sqrt(udH2[:, kf].sum(0)))
+    assert_close(o["dW_down"][:, tm(kf)], ref["dW_down_ref"][:, kf], "dW_down", propagated(dY2.T, uH2[:, kf]))
     assert_close(o["db_down"], ref["db_down"], "db_down")
     for key in ("Y", "dX", "dW_up", "dW_down"):       # normwise over everything
         g = o[key].float().cpu().numpy().astype(np.float64)
@@ -97,8 +105,46 @@ def compare_step(o, ref, w: FFNWorkload, act24: bool):
 
 
 def oracle_step(inp, act24):
-    return O.ffn_step(bits_of(inp["X"]), bits_of(inp["W_up"]), inp["b_up"].cpu().numpy(), bits_of(inp["W_down"]),
-                      inp["b_down"].cpu().numpy(), bits_of(inp["dY"]), act24=act24)
+    r = O.ffn_step(bits_of(inp["X"]), bits_of(inp["W_up"]), inp["b_up"].cpu().numpy(), bits_of(inp["W_down"]),
+                   inp["b_down"].cpu().numpy(), bits_of(inp["dY"]), act24=act24)
+    r["X"], r["dY"] = bits_of(inp["X"]), bits_of(inp["dY"])
+    return r
+
+
+def integer_inputs(w: FFNWorkload, seed: int):
+    """Values in {-1, 0, 1} (bias in {-2..2}): every product and partial sum of the
+    step is a small integer, exact in fp32 in any order, so GPU and oracle must agree
+    bit for bit on every output (bf16 roundings of identical fp32 values included)."""
+    from synth24 import small_int_bf16
+    dev = "cuda"
+    return {
+        "X": small_int_bf16((w.M, w.d), -1, 1, seed, 1, dev),
+        "W_up": small_int_bf16((w.ffn, w.d), -1, 1, seed, 2, dev),
+        "W_down": small_int_bf16((w.d, w.ffn), -1, 1, seed, 3, dev),
+        "dY": small_int_bf16((w.M, w.d), -1, 1, seed, 6, dev),
+        "b_up": small_int_bf16((w.ffn,), -2, 2, seed, 4, dev).float(),
+        "b_down": small_int_bf16((w.d,), -2, 2, seed, 5, dev).float(),
+    }
+
+
+@pytest.mark.parametrize("act24", [False, True])
+@pytest.mark.parametrize("shape", [(520, 264, 392), (4096, 768, 3072)])
+def test_ffn_step_integer_inputs_bit_exact(P, shape, act24):
+    M, d, ffn = shape
+    w = FFNWorkload("int", M, d, ffn, 1.0)
+    inp = integer_inputs(w, seed=3)
+    o = run_gpu(P, inp, act24)
+    ref = oracle_step(inp, act24)
+    # every fp32 sum stays far below 2**24, so the exact result is order-independent
+    assert np.abs(ref["dW_up_ref"]).max() < 2 ** 20 and np.abs(ref["dW_down_ref"]).max() < 2 ** 20
+    from tests.p24_testutil import assert_bits_equal
+    assert_bits_equal(bits_of(o["H"]), ref["H_used"] if act24 else ref["H"], "H")
+    assert_bits_equal(bits_of(o["Y"]), ref["Y"], "Y")
+    assert_bits_equal(bits_of(o["dX"]), ref["dX"], "dX")
+    assert_bits_equal(bits_of(o["dW_up"]), ref["dW_up"], "dW_up")
+    assert_bits_equal(bits_of(o["dW_down"]), ref["dW_down"], "dW_down")
+    assert np.array_equal(o["db_up"].cpu().numpy(), ref["db_up"])
+    assert np.array_equal(o["db_down"].cpu().numpy(), ref["db_down"])
 
 
 @pytest.mark.parametrize("act24", [False, True])
@@ -144,26 +190,34 @@ def test_ffn_step_70b_bench_workload_sampled(P):
         assert np.all(np.maximum(g, r)[flip] <= 1e-3 * scale)
         return flip
 
+    Wd2 = O.bf16_to_f32(O.decompress24(dn_v, dn_m, w.ffn)) ** 2           # [d, ffn]
+    WubT2 = O.bf16_to_f32(O.decompress24(upT_v, upT_m, w.ffn)) ** 2       # [d, ffn]
     # token rows: H, Y, dX
     H_r, H_b = O.spmm24_fwd(X[ms], up_v, up_m, w.d, relu=True)
     assert_close(o["H"][tm(ms)], H_r, "H rows")
     Y_r, _ = O.spmm24_fwd(H_b, dn_v, dn_m, w.ffn)
-    assert_close(o["Y"][tm(ms)], Y_r, "Y rows")
+    assert_close(o["Y"][tm(ms)], Y_r, "Y rows", propagated(ulp_bf16(H_b) ** 2, Wd2.T))
     _, dH_b = O.spmm24_bwd_dx(dY[ms], dnT_v, dnT_m, w.d, gate=H_b)
     dX_r, _ = O.spmm24_bwd_dx(dH_b, upT_v, upT_m, w.ffn)
     keep = ~gate_flips(o["H"][tm(ms)], H_b, H_r).any(axis=1)
     assert keep.sum() >= len(ms) - 2
-    assert_close(o["dX"][tm(ms[keep])], dX_r[keep], "dX rows")
+    assert_close(o["dX"][tm(ms[keep])], dX_r[keep], "dX rows",
+                 propagated(ulp_bf16(dH_b[keep]) ** 2, WubT2.T))
+    del Wd2, WubT2
     # weight rows: dW_up[fs, :] needs dH[:, fs] over all tokens
     Hc_r, Hc_b = O.spmm24_fwd(X, up_v[fs], up_m[fs], w.d, relu=True)        # H[:, fs]
     _, dHc_b = O.spmm24_bwd_dx(dY, dnT_v[fs], dnT_m[fs], w.d, gate=Hc_b)     # dH[:, fs]
     dWu_r, _ = O.masked_dw(dHc_b, X, up_m[fs])
     keep = ~gate_flips(o["H"][:, tm(fs)], Hc_b, Hc_r).any(axis=0)
     assert keep.sum() >= len(fs) - 2
-    assert_close(o["dW_up"][tm(fs[keep])], dWu_r[keep], "dW_up rows")
-    assert_close(o["db_up"][tm(fs[keep])], O.colsum(dHc_b)[keep], "db_up entries")
+    udH2 = ulp_bf16(dHc_b) ** 2
+    X2 = O.bf16_to_f32(X) ** 2
+    assert_close(o["dW_up"][tm(fs[keep])], dWu_r[keep], "dW_up rows", propagated(udH2[:, keep].T, X2))
+    assert_close(o["db_up"][tm(fs[keep])], O.colsum(dHc_b)[keep], "db_up entries",
+                 4 * np.sqrt(udH2[:, keep].sum(0)))
     # dW_down[ns, :] = dY[:, ns]^T H on the mask: needs the oracle's whole H
     _, H_all = O.spmm24_fwd(X, up_v, up_m, w.d, relu=True)
     dWd_r, _ = O.masked_dw(dY[:, ns], H_all, dn_m[ns])
-    assert_close(o["dW_down"][tm(ns)], dWd_r, "dW_down rows")
+    dY2 = O.bf16_to_f32(dY[:, ns]) ** 2
+    assert_close(o["dW_down"][tm(ns)], dWd_r, "dW_down rows", propagated(dY2.T, ulp_bf16(H_all) ** 2))
     assert_close(o["db_down"][tm(ns)], O.colsum(dY[:, ns]), "db_down entries")
