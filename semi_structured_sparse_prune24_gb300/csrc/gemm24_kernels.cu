@@ -17,6 +17,12 @@
 // sparse backward); "To 2:4 Sparsity and Beyond" abstract (2:4 weights and
 // sparse activations in all FFN matmuls).
 //
+// Both kernels run as clusters of 2 CTAs (one per SM). The two CTAs of a cluster
+// own adjacent A tiles and share one B tile: each loads half of the B tile and
+// TMA-multicasts it to both, which halves the B traffic from L2. A stage is
+// refilled only after both CTAs' MMAs released it (the MMA commit is multicast
+// to the empty barrier of both CTAs).
+//
 // Roles (warp index): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 epilogue
 // (warp w reads TMEM lanes 32*(w%4)..+31), 6-9 (spmm only) metadata movers:
 // smem -> registers -> TMEM, replacing rows past the matrix with a legal pattern.
@@ -144,7 +150,7 @@ __device__ __forceinline__ uint32_t meta_col(int s, int j) {
 }
 
 template <int BN, int STAGES, bool kTransOut>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
   using L = SpmmSmem<BN, STAGES>;
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // one MMA commit from each CTA of the cluster
       mbar_init(&meta_ready[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
@@ -188,25 +194,29 @@ __global__ void __launch_bounds__(320, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int ta, tb;
         tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+        ta = 2 * ta + rank;
         for (int kb = 0; kb < p.nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], L::kTx);
           tma_load_2d(smem + L::kOffA + s * L::kA, &tmA, &full[s], kb * 32, ta * kBM);
-          tma_load_2d(smem + L::kOffB + s * L::kB, &tmB, &full[s], kb * 64, tb * BN);
+          tma_load_2d_mc(smem + L::kOffB + s * L::kB + rank * (L::kB / 2), &tmB, &full[s], kb * 64,
+                         tb * BN + rank * (BN / 2), 0x3);
           tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &full[s], (kb >> 1) * 16, ta * kBM);
         }
       }
@@ -221,7 +231,7 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------ MMA issuer
     uint32_t it = 0, tl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tl) {
+    for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
       const int b = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) { ok = false; break; }
@@ -245,7 +255,7 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t bdesc = smem_desc(b_base + j * 64, 16, 1024, kSwizzle128B);
             tc_mma_sp_f16(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
           }
-          tc_commit(&empty[s]);
+          tc_commit_mc(&empty[s], 0x3);
         }
         __syncwarp();
       }
@@ -269,9 +279,10 @@ __global__ void __launch_bounds__(320, 1)
     const int h = (lane >> 3) & 1;
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int t = cid; t < p.num_tiles && ok; t += ncl) {
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      ta = 2 * ta + rank;
       const bool okA = ta * kBM + rowA < p.rowsA;
       const bool okB = ta * kBM + rowB < p.rowsA;
       for (int kb = 0; kb < p.nkb; ++kb, ++it) {
@@ -298,9 +309,10 @@ __global__ void __launch_bounds__(320, 1)
     const int q = warp & 3;
     uint16_t* stage = reinterpret_cast<uint16_t*>(smem + L::kOffStage) + q * 32 * 32;
     uint32_t tl = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
+    for (int t = cid; t < p.num_tiles; t += ncl, ++tl) {
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      ta = 2 * ta + rank;
       const int b = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
@@ -391,7 +403,7 @@ __global__ void __launch_bounds__(320, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the peer may still multicast into / arrive on this CTA until here
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
@@ -412,7 +424,7 @@ struct DwSmem {
 };
 
 template <int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     dw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const DwParams p) {
   using L = DwSmem<STAGES>;
   constexpr int BN = 256;
@@ -432,7 +444,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // one MMA commit from each CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -449,17 +461,20 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int ta, tb;
         tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+        ta = 2 * ta + rank;
         for (int kb = 0; kb < p.nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -468,7 +483,8 @@ __global__ void __launch_bounds__(192, 1)
           uint8_t* a = smem + L::kOffA + s * L::kA;
           uint8_t* b = smem + L::kOffB + s * L::kB;
           for (int i = 0; i < 2; ++i) tma_load_2d(a + i * 8192, &tmA, &full[s], ta * kBM + i * 64, kb * 64);
-          for (int i = 0; i < 4; ++i) tma_load_2d(b + i * 8192, &tmB, &full[s], tb * BN + i * 64, kb * 64);
+          for (int i = 2 * rank; i < 2 * rank + 2; ++i)
+            tma_load_2d_mc(b + i * 8192, &tmB, &full[s], tb * BN + i * 64, kb * 64, 0x3);
         }
       }
       const uint32_t n_drain = it < STAGES ? it : STAGES;
@@ -480,7 +496,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     uint32_t it = 0, tl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tl) {
+    for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
       const int b = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) break;
@@ -500,7 +516,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t bdesc = smem_desc(b_base + kk * 2048, 8192, 1024, kSwizzle128B);
             tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0);
           }
-          tc_commit(&empty[s]);
+          tc_commit_mc(&empty[s], 0x3);
         }
         __syncwarp();
       }
@@ -516,9 +532,10 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int q = warp & 3;
     uint32_t tl = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
+    for (int t = cid; t < p.num_tiles; t += ncl, ++tl) {
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      ta = 2 * ta + rank;
       const int b = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
@@ -564,7 +581,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the peer may still multicast into / arrive on this CTA until here
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
@@ -620,7 +637,7 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const int grid = std::min(p.num_tiles, num_sms());
+  const int grid = 2 * std::min(p.num_tiles, num_sms() / 2);  // clusters of 2
   kern<<<grid, 320, smem, s>>>(a, b, e, p);
   count_launch();
   return cudaGetLastError();
@@ -635,10 +652,10 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   p.rowsA = static_cast<int>(A.rows);
   p.rowsB = static_cast<int>(rowsB);
   p.K = static_cast<int>(A.cols);
-  p.tilesA = static_cast<int>((A.rows + kBM - 1) / kBM);
+  p.tilesA = static_cast<int>((A.rows + 2 * kBM - 1) / (2 * kBM));  // A tile pairs (one per cluster)
   p.tilesB = static_cast<int>((rowsB + kSpBN - 1) / kSpBN);
   p.num_tiles = p.tilesA * p.tilesB;
-  p.group = std::min(p.tilesA, 16);
+  p.group = std::min(p.tilesA, 8);
   p.nkb = static_cast<int>((A.cols + 63) / 64);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.ldo = ldo;
@@ -656,7 +673,7 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   CUtensorMap ta, tb, te;
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 32, kBM,
                    CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64, kSpBN,
+      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64, kSpBN / 2,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -676,10 +693,10 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.M = static_cast<int>(M);
-  p.tilesA = static_cast<int>((N + kBM - 1) / kBM);
+  p.tilesA = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));  // A tile pairs (one per cluster)
   p.tilesB = static_cast<int>((K + 255) / 256);
   p.num_tiles = p.tilesA * p.tilesB;
-  p.group = std::min(p.tilesA, 16);
+  p.group = std::min(p.tilesA, 8);
   p.nkb = static_cast<int>((M + 63) / 64);
   p.out = static_cast<__nv_bfloat16*>(dW);
   p.ldo = lddw;
@@ -696,7 +713,7 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const int grid = std::min(p.num_tiles, num_sms());
+  const int grid = 2 * std::min(p.num_tiles, num_sms() / 2);  // clusters of 2
   kern<<<grid, 192, smem, s>>>(ta, tb, p);
   count_launch();
   return cudaGetLastError();
