@@ -194,6 +194,33 @@ size_t p24_colsum_workspace_size(int64_t M, int64_t N);
 int p24_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out,
                void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * p24_colsum_noalloc -- p24_colsum for callers that cannot allocate device
+ * memory. The pages have no counterpart to this call; it exists for integration.
+ *
+ * Who needs it: a caller that has no device allocator of its own to call, e.g.
+ * C code embedded in a framework whose memory pool already owns the GPU's memory
+ * (a cudaMalloc behind the pool's back fails or fragments it), or code on a path
+ * where a cudaMalloc/cudaFree, which can synchronise the device, would stall the
+ * asynchronous pipeline around it.
+ *
+ * How: the partial sums go to a fixed array of P24_COLSUM_NOALLOC_SCRATCH_FLOATS
+ * floats (4 MiB) inside the library, held on every GPU that loads the library
+ * until the process exits. The call allocates and frees nothing.
+ *   G, M, N, ldg, out : as p24_colsum. Results equal p24_colsum's up to fp32
+ *                       rounding (for very wide N fewer row slabs are used);
+ *                       repeated calls with the same input are bit-identical.
+ *   N > P24_COLSUM_NOALLOC_MAX_COLS is rejected with P24_ENOSPACE (nothing launched).
+ * The first call on each device looks up the scratch array's device address
+ * (with that device current); make that first call before any stream capture.
+ * Every call uses the same scratch array and leaves its partial sums there;
+ * calls whose kernels overlap on the GPU (different streams, no ordering) race
+ * on it and give wrong sums: order them on one stream or with events.
+ */
+#define P24_COLSUM_NOALLOC_SCRATCH_FLOATS (1 << 20)
+#define P24_COLSUM_NOALLOC_MAX_COLS P24_COLSUM_NOALLOC_SCRATCH_FLOATS
+int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, void* stream);
+
 /* Flags of ffn24_step. */
 #define P24_STEP_ACT24 0x1u /* 2:4-prune ReLU(up) and feed it as the sparse operand of down */
 

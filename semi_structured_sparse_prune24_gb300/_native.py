@@ -43,7 +43,7 @@ class p24_ffn_args(C.Structure):
 def _load() -> C.CDLL:
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"libprune24 is not built ({_LIB_PATH} missing): run __graft_entry__.build() "
-                          "or python -m semi_structured_sparse_prune24_gb300.build")
+                          "or python semi_structured_sparse_prune24_gb300/build.py")
     L = C.CDLL(_LIB_PATH)
     i64, vp, u32, sz, i32 = C.c_int64, C.c_void_p, C.c_uint32, C.c_size_t, C.c_int
     sp = C.POINTER(p24_sparse)
@@ -59,6 +59,7 @@ def _load() -> C.CDLL:
         "masked_dw_gemm": (i32, [vp, i64, vp, i64, i64, sp, vp, i64, vp]),
         "p24_colsum_workspace_size": (sz, [i64, i64]),
         "p24_colsum": (i32, [vp, i64, i64, i64, vp, vp, sz, vp]),
+        "p24_colsum_noalloc": (i32, [vp, i64, i64, i64, vp, vp]),
         "ffn24_workspace_size": (sz, [i64, i64, i64, u32]),
         "ffn24_step": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp]),
         "ffn24_step_traced": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp, C.POINTER(vp), i32]),
@@ -253,6 +254,14 @@ def p24_colsum(G: torch.Tensor, out: torch.Tensor | None = None, ws: torch.Tenso
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=G.device)
     _check(lib.p24_colsum(G.data_ptr(), M, N, ldg, out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
                           _stream(stream)), "p24_colsum")
+    return out
+
+
+def p24_colsum_noalloc(G: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Column sums with the library's fixed device scratch (no workspace; see include/prune24.h)."""
+    M, N, ldg = _mat(G, name="G")
+    out = torch.empty(N, dtype=torch.float32, device=G.device) if out is None else out
+    _check(lib.p24_colsum_noalloc(G.data_ptr(), M, N, ldg, out.data_ptr(), _stream(stream)), "p24_colsum_noalloc")
     return out
 
 

@@ -2,7 +2,7 @@
 
 Each .cu under csrc/ is compiled in parallel to an object file under _build/,
 then all are linked into semi_structured_sparse_prune24_gb300/_lib/libprune24.so.
-Nothing is installed outside the repository. Run: python -m semi_structured_sparse_prune24_gb300.build
+Nothing is installed outside the repository. Run: python semi_structured_sparse_prune24_gb300/build.py
 """
 from __future__ import annotations
 

@@ -235,6 +235,14 @@ int p24_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, voi
   return cuda_status(launch_colsum(G, M, N, ldg, out, static_cast<float*>(ws), as_stream(stream)));
 }
 
+int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, void* stream) {
+  P24_TRY(check_dense(G, M, N, ldg));
+  if (N > 0 && !out) return P24_EINVAL;
+  if (N > 0 && !aligned16(out)) return P24_EALIGN;
+  if (N > P24_COLSUM_NOALLOC_MAX_COLS) return P24_ENOSPACE;
+  return cuda_status(launch_colsum_noalloc(G, M, N, ldg, out, as_stream(stream)));
+}
+
 size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags) {
   if (M < 0 || d < 0 || ffn < 0) return 0;
   StepLayout L;

@@ -18,6 +18,9 @@ cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwd
 cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s);
 int64_t colsum_slabs(int64_t M);
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s);
+// Same sums with the library's fixed device scratch instead of a caller workspace.
+constexpr int64_t kNoAllocColsumScratch = int64_t(1) << 20;  // floats (4 MiB per GPU)
+cudaError_t launch_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, cudaStream_t s);
 
 // ---- tensor-core GEMMs (gemm24_kernels.cu) ----
 struct EpiArgs {

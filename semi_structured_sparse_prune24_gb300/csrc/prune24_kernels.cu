@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "p24_internal.h"
 
@@ -295,6 +296,11 @@ __global__ void colsum_final_kernel(const float* __restrict__ part, int64_t S, i
   out[col] = a;
 }
 
+// Scratch of p24_colsum_noalloc: a fixed device array, so that the call needs
+// no allocation. Every GPU that loads the library holds it until the process
+// exits. All calls share it (calls that overlap on the GPU race on it).
+__device__ __align__(256) float g_colsum_scratch[kNoAllocColsumScratch];
+
 inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n < 1 ? 1 : n) : 65535); }
 
 }  // namespace
@@ -366,6 +372,50 @@ int64_t colsum_slabs(int64_t M) {
   if (S > 1024) S = 1024;
   if (S < 1) S = 1;
   return S;
+}
+
+// Device address of g_colsum_scratch on the current device. Looked up once per
+// device (cudaGetSymbolAddress, with that device current) on first use.
+float* noalloc_colsum_scratch(cudaError_t* err) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static float* addr[kMaxDevices] = {};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_colsum_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<float*>(p);
+  }
+  return addr[dev];
+}
+
+cudaError_t launch_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  if (M == 0) return cudaMemsetAsync(out, 0, N * sizeof(float), s);
+  cudaError_t err = cudaSuccess;
+  float* ws = noalloc_colsum_scratch(&err);
+  if (!ws) return err;
+  // as many row slabs as the scratch holds partial rows for, at most the usual count
+  int64_t S = colsum_slabs(M);
+  if (S * N > kNoAllocColsumScratch) S = kNoAllocColsumScratch / N;
+  if (S < 1) return cudaErrorInvalidValue;  // rejected on the host before this point
+  const int64_t rps = (M + S - 1) / S;
+  dim3 grid(static_cast<unsigned>((N + 511) / 512), static_cast<unsigned>(S));
+  colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), M, N, ldg, rps, ws);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colsum_final_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(ws, S, N, out);
+  count_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s) {
