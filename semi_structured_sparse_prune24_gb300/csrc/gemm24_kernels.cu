@@ -122,22 +122,29 @@ __device__ __forceinline__ void tc_st_32x32b_x1(uint32_t taddr, uint32_t a) {
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// ---------------------------------------------------------------- sparse GEMM
-// Per stage (64 logical K): A 128 rows x 32 compressed bf16 (64 B rows,
-// 64B swizzle), B BN rows x 64 bf16 (128 B rows, 128B swizzle), metadata
-// 128 rows x 16 B (the 8 bytes of this stage sit at (kb & 1) * 8).
+// ---------------------------------------------------------------- sparse GEMM (CTA pair)
+// A cluster of 2 CTAs computes each 256 x BN output tile with pair MMAs
+// (tcgen05.mma.sp.cta_group::2, M = 256). CTA c of the pair holds A rows
+// 128c..128c+127 of the tile and B rows c*BN/2..(c+1)*BN/2-1, so each SM stages
+// and reads only half of B; CTA 0 (the leader) issues the MMAs. Each CTA's TMEM
+// holds the accumulator rows and the metadata of its own 128 A rows, in the
+// single-CTA layout. The A and B loads of both CTAs complete on the leader's
+// `full` barrier; each CTA's metadata tile completes on its own `efull` barrier.
+// Per stage (64 logical K) per CTA: A 128 x 32 compressed bf16 (64 B rows, 64B
+// swizzle), B BN/2 x 64 bf16 (128 B rows, 128B swizzle), metadata 128 x 16 B
+// (the 8 bytes of this stage sit at (kb & 1) * 8).
 template <int BN, int STAGES>
 struct SpmmSmem {
-  static constexpr int kA = kBM * 64;   // bytes per stage
-  static constexpr int kB = BN * 128;
+  static constexpr int kA = kBM * 64;  // bytes per stage
+  static constexpr int kB = (BN / 2) * 128;
   static constexpr int kE = kBM * 16;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
   static constexpr int kOffE = kOffB + STAGES * kB;
   static constexpr int kOffStage = kOffE + STAGES * kE;  // epilogue transpose, 4 warps x 32x32 bf16
   static constexpr int kOffBar = kOffStage + 4 * 32 * 32 * 2;
-  static constexpr int kBytes = kOffBar + 8 * (4 * STAGES + 4) + 16;
-  static constexpr int kTx = kA + kB + kE;
+  static constexpr int kBytes = kOffBar + 8 * (4 * STAGES + 5) + 16;
+  static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
 };
 
 // TMEM column of the metadata of MMA j (0/1) of stage s: 8-column slots in the
@@ -149,24 +156,57 @@ __device__ __forceinline__ uint32_t meta_col(int s, int j) {
   return k < kGap ? BN + 8 * k : 256 + BN + 8 * (k - kGap);
 }
 
+// ---- pair (cta_group::2) forms
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {  // same smem offset in cluster rank 0
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(p)));
+  return r;
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_sp_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t e_tmem,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(e_tmem), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 template <int BN, int STAGES, bool kTransOut>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
   using L = SpmmSmem<BN, STAGES>;
   constexpr int kAccCols = 256;  // accumulator buffer b starts at column 256 * b
-  static_assert(BN <= 256 && BN % 8 == 0 && 2 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
-  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, /*sparse=*/true, false, false);
+  static_assert(BN <= 256 && BN % 16 == 0 && 2 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
+  constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, false);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  uint64_t* empty = full + STAGES;
-  uint64_t* meta_ready = empty + STAGES;
-  uint64_t* acc_full = meta_ready + STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;         // [2]
-  uint64_t* spare = acc_empty + 2;            // [STAGES] unused
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + STAGES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // leader's is used
+  uint64_t* efull = full + STAGES;                                    // own metadata tile landed
+  uint64_t* empty = efull + STAGES;                                   // leader's commit, both CTAs
+  uint64_t* meta_ready = empty + STAGES;                              // leader's is used (8 arrivals)
+  uint64_t* acc_full = meta_ready + STAGES;                           // [2] leader's commit, both CTAs
+  uint64_t* acc_empty = acc_full + 2;                                 // [2] leader's is used (8 arrivals)
+  uint64_t* spare = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -175,12 +215,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // one MMA commit from each CTA of the cluster
-      mbar_init(&meta_ready[s], 4);
+      mbar_init(&efull[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&meta_ready[s], 8);  // 4 mover warps x 2 CTAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], 8);   // 4 epilogue warps x 2 CTAs
     }
     mbar_init(spare, 1);
     *abort_flag = 0;
@@ -189,19 +230,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmE);
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+  if (warp == 1) {  // pair allocation: one warp of each CTA, same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -213,64 +257,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], L::kTx);
-          tma_load_2d(smem + L::kOffA + s * L::kA, &tmA, &full[s], kb * 32, ta * kBM);
-          tma_load_2d_mc(smem + L::kOffB + s * L::kB + rank * (L::kB / 2), &tmB, &full[s], kb * 64,
-                         tb * BN + rank * (BN / 2), 0x3);
-          tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &full[s], (kb >> 1) * 16, ta * kBM);
+          if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
+          mbar_arrive_expect_tx(&efull[s], L::kE);
+          const uint32_t fullL = leader_addr(&full[s]);
+          tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 32, ta * kBM);
+          tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 64, tb * BN + rank * (BN / 2));
+          tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &efull[s], (kb >> 1) * 16, ta * kBM);
         }
       }
-      // Drain: every issued load must land before the CTA may exit.
+      // Drain: the last issued loads must land before the CTA may exit.
       const uint32_t n_drain = it < STAGES ? it : STAGES;
       for (uint32_t i = 0; i < n_drain; ++i) {
         const uint32_t j = it - 1 - i;
-        p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
+        p24_wait_quiet(&efull[j % STAGES], (j / STAGES) & 1);
+        if (leader) p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    uint32_t it = 0, tl = 0;
-    bool ok = true;
-    for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
-      const int b = tl & 1;
-      const uint32_t aph = (tl >> 1) & 1;
-      if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + b * kAccCols;
-      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!p24_wait(&full[s], ph, abort_flag, p.status) ||
-            !p24_wait(&meta_ready[s], ph, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
+    // ------------------------------------------------ MMA issuer (leader CTA only)
+    if (leader) {
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
+        const int b = tl & 1;
+        const uint32_t aph = (tl >> 1) & 1;
+        if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
-          const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint64_t adesc = smem_desc(a_base + j * 32, 16, 512, kSwizzle64B);
-            const uint64_t bdesc = smem_desc(b_base + j * 64, 16, 1024, kSwizzle128B);
-            tc_mma_sp_f16(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
+        const uint32_t d_tmem = tmem + b * kAccCols;
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!p24_wait(&full[s], ph, abort_flag, p.status) ||
+              !p24_wait(&meta_ready[s], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
-          tc_commit_mc(&empty[s], 0x3);
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
+            const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint64_t adesc = smem_desc(a_base + j * 32, 16, 512, kSwizzle64B);
+              const uint64_t bdesc = smem_desc(b_base + j * 64, 16, 1024, kSwizzle128B);
+              tc_mma_sp_pair(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
+            }
+            tc_commit_pair(&empty[s], 0x3);
+          }
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair(&acc_full[b], 0x3);
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&acc_full[b]);
+      // Make sure no MMA is still running before TMEM is released.
+      if (lane == 0) {
+        tc_commit_pair(spare, 0x1);
+        p24_wait_quiet(spare, 0);
+      }
       __syncwarp();
     }
-    // Make sure no MMA is still running before TMEM is released.
-    if (lane == 0) {
-      tc_commit(spare);
-      p24_wait_quiet(spare, 0);
-    }
-    __syncwarp();
   } else if (warp >= 6) {
-    // ------------------------------------------------ metadata movers
+    // ------------------------------------------------ metadata movers (both CTAs)
     // Lane l of quarter q fills TMEM lane 32q + l: rows rA = 32q + (l & 16) + (l & 7)
     // and rA + 8, K-half h = (l >> 3) & 1 of each MMA's 32 metadata bits.
     const int q = warp & 3;
@@ -288,7 +336,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       for (int kb = 0; kb < p.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!p24_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
+        if (!p24_wait(&efull[s], ph, abort_flag, p.status)) { ok = false; break; }
         const uint8_t* e = smem + L::kOffE + s * L::kE + (kb & 1) * 8;
         const uint2 ea = *reinterpret_cast<const uint2*>(e + rowA * 16);
         const uint2 eb = *reinterpret_cast<const uint2*>(e + rowB * 16);
@@ -301,11 +349,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&meta_ready[s]);
+        if (lane == 0) arrive_cluster(leader_addr(&meta_ready[s]));
       }
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2-5)
+    // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
     const int q = warp & 3;
     uint16_t* stage = reinterpret_cast<uint16_t*>(smem + L::kOffStage) + q * 32 * 32;
     uint32_t tl = 0;
@@ -330,8 +378,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           for (int j = 0; j < 32; ++j) {
             float f = __uint_as_float(v[j]) + bias_v;
             if (p.relu) f = fmaxf(f, 0.f);
-            __nv_bfloat16 h = __float2bfloat16_rn(f);
-            stage[j * 32 + lane] = *reinterpret_cast<uint16_t*>(&h);
+            __nv_bfloat16 hv = __float2bfloat16_rn(f);
+            stage[j * 32 + lane] = *reinterpret_cast<uint16_t*>(&hv);
           }
           __syncwarp();
 #pragma unroll
@@ -398,14 +446,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
     }
   }
 
   tc_fence_before();
-  cluster_sync();  // the peer may still multicast into / arrive on this CTA until here
+  cluster_sync();  // the peer may still signal this CTA's barriers until here
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
 }
 
 // ---------------------------------------------------------------- masked dW GEMM
@@ -625,8 +674,8 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-constexpr int kSpBN = 224;
-constexpr int kSpStages = 4;
+constexpr int kSpBN = 192;
+constexpr int kSpStages = 8;
 constexpr int kDwStages = 4;
 
 template <bool kTrans>
