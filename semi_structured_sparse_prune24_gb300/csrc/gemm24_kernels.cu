@@ -130,13 +130,14 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 // holds the accumulator rows and the metadata of its own 128 A rows, in the
 // single-CTA layout. The A and B loads of both CTAs complete on the leader's
 // `full` barrier; each CTA's metadata tile completes on its own `efull` barrier.
-// Per stage (64 logical K) per CTA: A 128 x 32 compressed bf16 (64 B rows, 64B
-// swizzle), B BN/2 x 64 bf16 (128 B rows, 128B swizzle), metadata 128 x 16 B
-// (the 8 bytes of this stage sit at (kb & 1) * 8).
+// Per stage (128 logical K, 4 MMAs) per CTA: A 128 x 64 compressed bf16 (128 B
+// rows, 128B swizzle), B two boxes of BN/2 x 64 bf16 (128 B rows, 128B swizzle,
+// K 0-63 and 64-127), metadata 128 x 16 B (one 32-bit word per MMA per row).
 template <int BN, int STAGES>
 struct SpmmSmem {
-  static constexpr int kA = kBM * 64;  // bytes per stage
-  static constexpr int kB = (BN / 2) * 128;
+  static constexpr int kA = kBM * 128;  // bytes per stage
+  static constexpr int kBHalf = (BN / 2) * 128;  // one 64-K box of this CTA's B rows
+  static constexpr int kB = 2 * kBHalf;
   static constexpr int kE = kBM * 16;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
@@ -147,12 +148,12 @@ struct SpmmSmem {
   static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
 };
 
-// TMEM column of the metadata of MMA j (0/1) of stage s: 8-column slots in the
+// TMEM column of the metadata of MMA j (0-3) of stage s: 8-column slots in the
 // gaps after the two accumulator buffers ([BN, 256) and [256 + BN, 512)).
 template <int BN>
 __device__ __forceinline__ uint32_t meta_col(int s, int j) {
   constexpr int kGap = (256 - BN) / 8;  // slots per gap
-  const int k = 2 * s + j;
+  const int k = 4 * s + j;
   return k < kGap ? BN + 8 * k : 256 + BN + 8 * (k - kGap);
 }
 
@@ -162,8 +163,12 @@ __device__ __forceinline__ uint32_t leader_addr(const void* p) {  // same smem o
   asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(p)));
   return r;
 }
+// Arrive on a barrier of another CTA of the cluster. Default (CTA-scope release)
+// semantics: what the arrival publishes is TMEM state already completed by
+// tcgen05.wait::st / wait::ld and ordered by tcgen05 fences, so the costly
+// cluster-scope release of all prior memory operations is not needed.
 __device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y) {
   asm volatile(
@@ -194,7 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                 const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
   using L = SpmmSmem<BN, STAGES>;
   constexpr int kAccCols = 256;  // accumulator buffer b starts at column 256 * b
-  static_assert(BN <= 256 && BN % 16 == 0 && 2 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
+  static_assert(BN <= 256 && BN % 16 == 0 && 4 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
   constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, false);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -260,9 +265,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
           mbar_arrive_expect_tx(&efull[s], L::kE);
           const uint32_t fullL = leader_addr(&full[s]);
-          tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 32, ta * kBM);
-          tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 64, tb * BN + rank * (BN / 2));
-          tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &efull[s], (kb >> 1) * 16, ta * kBM);
+          tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 64, ta * kBM);
+          tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 128, tb * BN + rank * (BN / 2));
+          tma_load_2d_pair(smem + L::kOffB + s * L::kB + L::kBHalf, &tmB, fullL, kb * 128 + 64,
+                           tb * BN + rank * (BN / 2));
+          tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &efull[s], kb * 16, ta * kBM);
         }
       }
       // Drain: the last issued loads must land before the CTA may exit.
@@ -297,9 +304,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
             const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint64_t adesc = smem_desc(a_base + j * 32, 16, 512, kSwizzle64B);
-              const uint64_t bdesc = smem_desc(b_base + j * 64, 16, 1024, kSwizzle128B);
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc(a_base + j * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bdesc = smem_desc(b_base + (j >> 1) * L::kBHalf + (j & 1) * 64, 16, 1024, kSwizzle128B);
               tc_mma_sp_pair(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
             }
             tc_commit_pair(&empty[s], 0x3);
@@ -337,15 +344,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!p24_wait(&efull[s], ph, abort_flag, p.status)) { ok = false; break; }
-        const uint8_t* e = smem + L::kOffE + s * L::kE + (kb & 1) * 8;
-        const uint2 ea = *reinterpret_cast<const uint2*>(e + rowA * 16);
-        const uint2 eb = *reinterpret_cast<const uint2*>(e + rowB * 16);
+        const uint8_t* e = smem + L::kOffE + s * L::kE;
+        const uint4 ea = *reinterpret_cast<const uint4*>(e + rowA * 16);
+        const uint4 eb = *reinterpret_cast<const uint4*>(e + rowB * 16);
+        const uint32_t wa[4] = {ea.x, ea.y, ea.z, ea.w}, wb[4] = {eb.x, eb.y, eb.z, eb.w};
         const uint32_t sh = 16u * h;
-        const uint32_t a0 = okA ? (ea.x >> sh) & 0xFFFFu : 0x4444u, a1 = okA ? (ea.y >> sh) & 0xFFFFu : 0x4444u;
-        const uint32_t b0 = okB ? (eb.x >> sh) & 0xFFFFu : 0x4444u, b1 = okB ? (eb.y >> sh) & 0xFFFFu : 0x4444u;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        tc_st_32x32b_x1(tmem + lane_base + meta_col<BN>(s, 0), a0 | (b0 << 16));
-        tc_st_32x32b_x1(tmem + lane_base + meta_col<BN>(s, 1), a1 | (b1 << 16));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a = okA ? (wa[j] >> sh) & 0xFFFFu : 0x4444u;
+          const uint32_t b = okB ? (wb[j] >> sh) & 0xFFFFu : 0x4444u;
+          tc_st_32x32b_x1(tmem + lane_base + meta_col<BN>(s, j), a | (b << 16));
+        }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -675,7 +685,7 @@ int num_sms() {
 }
 
 constexpr int kSpBN = 192;
-constexpr int kSpStages = 8;
+constexpr int kSpStages = 4;
 constexpr int kDwStages = 4;
 
 template <bool kTrans>
@@ -705,7 +715,7 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   p.tilesB = static_cast<int>((rowsB + kSpBN - 1) / kSpBN);
   p.num_tiles = p.tilesA * p.tilesB;
   p.group = std::min(p.tilesA, 8);
-  p.nkb = static_cast<int>((A.cols + 63) / 64);
+  p.nkb = static_cast<int>((A.cols + 127) / 128);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.ldo = ldo;
   p.bias = epi.bias;
@@ -720,8 +730,8 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   if (A.cols == 0) return cudaErrorInvalidValue;
 
   CUtensorMap ta, tb, te;
-  if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 32, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 64, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64, kSpBN / 2,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16, kBM,
