@@ -132,19 +132,23 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 // `full` barrier; each CTA's metadata tile completes on its own `efull` barrier.
 // Per stage (128 logical K, 4 MMAs) per CTA: A 128 x 64 compressed bf16 (128 B
 // rows, 128B swizzle), B two boxes of BN/2 x 64 bf16 (128 B rows, 128B swizzle,
-// K 0-63 and 64-127), metadata 128 x 16 B (one 32-bit word per MMA per row).
+// K 0-63 and 64-127). Metadata comes in blocks of 4 stages (512 logical K):
+// 128 rows x 64 B (one 32-bit word per MMA per row), in a ring of its own, so
+// that a TMA row request carries 64 bytes instead of 16.
+constexpr int kEStages = 4;  // stages per metadata block
+constexpr int kEBufs = 2;    // metadata ring depth
 template <int BN, int STAGES>
 struct SpmmSmem {
   static constexpr int kA = kBM * 128;  // bytes per stage
   static constexpr int kBHalf = (BN / 2) * 128;  // one 64-K box of this CTA's B rows
   static constexpr int kB = 2 * kBHalf;
-  static constexpr int kE = kBM * 16;
+  static constexpr int kE = kBM * 16 * kEStages;  // bytes per metadata block
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
   static constexpr int kOffE = kOffB + STAGES * kB;
-  static constexpr int kOffStage = kOffE + STAGES * kE;  // epilogue transpose, 4 warps x 32x32 bf16
+  static constexpr int kOffStage = kOffE + kEBufs * kE;  // epilogue transpose, 4 warps x 32x32 bf16
   static constexpr int kOffBar = kOffStage + 4 * 32 * 32 * 2;
-  static constexpr int kBytes = kOffBar + 8 * (4 * STAGES + 5) + 16;
+  static constexpr int kBytes = kOffBar + 8 * (3 * STAGES + 2 * kEBufs + 5) + 16;
   static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
 };
 
@@ -205,10 +209,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // leader's is used
-  uint64_t* efull = full + STAGES;                                    // own metadata tile landed
-  uint64_t* empty = efull + STAGES;                                   // leader's commit, both CTAs
+  uint64_t* empty = full + STAGES;                                    // leader's commit, both CTAs
   uint64_t* meta_ready = empty + STAGES;                              // leader's is used (8 arrivals)
-  uint64_t* acc_full = meta_ready + STAGES;                           // [2] leader's commit, both CTAs
+  uint64_t* efull = meta_ready + STAGES;                              // [kEBufs] own metadata block landed
+  uint64_t* eempty = efull + kEBufs;                                  // [kEBufs] own movers done with it
+  uint64_t* acc_full = eempty + kEBufs;                               // [2] leader's commit, both CTAs
   uint64_t* acc_empty = acc_full + 2;                                 // [2] leader's is used (8 arrivals)
   uint64_t* spare = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + 1);
@@ -220,9 +225,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&efull[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&meta_ready[s], 8);  // 4 mover warps x 2 CTAs
+    }
+    for (int e = 0; e < kEBufs; ++e) {
+      mbar_init(&efull[e], 1);
+      mbar_init(&eempty[e], 4);      // this CTA's 4 mover warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -252,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, eit = 0;
       bool ok = true;
       for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int ta, tb;
@@ -261,23 +269,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         for (int kb = 0; kb < p.nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          if (kb % kEStages == 0) {  // next metadata block
+            const int e = eit % kEBufs;
+            if (!p24_wait(&eempty[e], ((eit / kEBufs) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(&efull[e], L::kE);
+            tma_load_2d(smem + L::kOffE + e * L::kE, &tmE, &efull[e], (kb / kEStages) * 64, ta * kBM);
+            ++eit;
+          }
           if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
-          mbar_arrive_expect_tx(&efull[s], L::kE);
           const uint32_t fullL = leader_addr(&full[s]);
           tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 64, ta * kBM);
           tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 128, tb * BN + rank * (BN / 2));
           tma_load_2d_pair(smem + L::kOffB + s * L::kB + L::kBHalf, &tmB, fullL, kb * 128 + 64,
                            tb * BN + rank * (BN / 2));
-          tma_load_2d(smem + L::kOffE + s * L::kE, &tmE, &efull[s], kb * 16, ta * kBM);
         }
       }
       // Drain: the last issued loads must land before the CTA may exit.
       const uint32_t n_drain = it < STAGES ? it : STAGES;
       for (uint32_t i = 0; i < n_drain; ++i) {
         const uint32_t j = it - 1 - i;
-        p24_wait_quiet(&efull[j % STAGES], (j / STAGES) & 1);
         if (leader) p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
+      }
+      const uint32_t e_drain = eit < kEBufs ? eit : kEBufs;
+      for (uint32_t i = 0; i < e_drain; ++i) {
+        const uint32_t j = eit - 1 - i;
+        p24_wait_quiet(&efull[j % kEBufs], (j / kEBufs) & 1);
       }
     }
   } else if (warp == 1) {
@@ -332,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     const int rowA = q * 32 + (lane & 16) + (lane & 7);
     const int rowB = rowA + 8;
     const int h = (lane >> 3) & 1;
-    uint32_t it = 0;
+    uint32_t it = 0, eit = 0;
     bool ok = true;
     for (int t = cid; t < p.num_tiles && ok; t += ncl) {
       int ta, tb;
@@ -343,10 +360,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       for (int kb = 0; kb < p.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!p24_wait(&efull[s], ph, abort_flag, p.status)) { ok = false; break; }
-        const uint8_t* e = smem + L::kOffE + s * L::kE;
-        const uint4 ea = *reinterpret_cast<const uint4*>(e + rowA * 16);
-        const uint4 eb = *reinterpret_cast<const uint4*>(e + rowB * 16);
+        const int eb_i = eit % kEBufs;
+        if (kb % kEStages == 0 &&
+            !p24_wait(&efull[eb_i], (eit / kEBufs) & 1, abort_flag, p.status)) { ok = false; break; }
+        // the stage's TMEM metadata slots are free once the MMAs of their previous use completed
+        if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+        const uint8_t* e = smem + L::kOffE + eb_i * L::kE + (kb % kEStages) * 16;
+        const uint4 ea = *reinterpret_cast<const uint4*>(e + rowA * 64);
+        const uint4 eb = *reinterpret_cast<const uint4*>(e + rowB * 64);
         const uint32_t wa[4] = {ea.x, ea.y, ea.z, ea.w}, wb[4] = {eb.x, eb.y, eb.z, eb.w};
         const uint32_t sh = 16u * h;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -360,6 +381,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_cluster(leader_addr(&meta_ready[s]));
+        if (kb % kEStages == kEStages - 1 || kb == p.nkb - 1) {  // done with this metadata block
+          if (lane == 0) mbar_arrive(&eempty[eb_i]);
+          ++eit;
+        }
       }
     }
   } else {
@@ -734,7 +759,7 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64, kSpBN / 2,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16, kBM,
+      !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   return transposed_out ? run_spmm<true>(ta, tb, te, p, s) : run_spmm<false>(ta, tb, te, p, s);
