@@ -702,6 +702,30 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Clusters of `cluster` CTAs of this kernel that can be resident at once (GPCs
+// need not divide evenly into clusters, so this can be below SMs / cluster).
+// A persistent grid larger than this would leave whole clusters for a second wave.
+template <class Kern>
+int max_active_clusters(Kern kern, int cluster, int threads, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();  // clear; fall back to the SM count
+    return 0;
+  }
+  return n;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -721,7 +745,9 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const int grid = 2 * std::min(p.num_tiles, num_sms() / 2);  // clusters of 2
+  int clusters = max_active_clusters(kern, 2, 320, smem);
+  if (clusters == 0) clusters = num_sms() / 2;
+  const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
   kern<<<grid, 320, smem, s>>>(a, b, e, p);
   count_launch();
   return cudaGetLastError();
@@ -797,7 +823,9 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const int grid = 2 * std::min(p.num_tiles, num_sms() / 2);  // clusters of 2
+  int clusters = max_active_clusters(kern, 2, 192, smem);
+  if (clusters == 0) clusters = num_sms() / 2;
+  const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
   kern<<<grid, 192, smem, s>>>(ta, tb, p);
   count_launch();
   return cudaGetLastError();
