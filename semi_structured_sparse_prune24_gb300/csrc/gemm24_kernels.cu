@@ -63,6 +63,7 @@ struct SpmmParams {
   uint8_t* a24_meta;
   int64_t a24_ldm;
   int* status;
+  int b3d;  // B map is 3-D: {64 K, rows, K / 64}; one load brings both 64-K halves of a stage
 };
 
 struct DwParams {
@@ -181,6 +182,14 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y,
+                                                 int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 __device__ __forceinline__ void tc_mma_sp_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t e_tmem,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -280,9 +289,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
           const uint32_t fullL = leader_addr(&full[s]);
           tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 64, ta * kBM);
-          tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 128, tb * BN + rank * (BN / 2));
-          tma_load_2d_pair(smem + L::kOffB + s * L::kB + L::kBHalf, &tmB, fullL, kb * 128 + 64,
-                           tb * BN + rank * (BN / 2));
+          if (p.b3d) {
+            tma_load_3d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, 0, tb * BN + rank * (BN / 2), kb * 2);
+          } else {
+            tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 128, tb * BN + rank * (BN / 2));
+            tma_load_2d_pair(smem + L::kOffB + s * L::kB + L::kBHalf, &tmB, fullL, kb * 128 + 64,
+                             tb * BN + rank * (BN / 2));
+          }
         }
       }
       // Drain: the last issued loads must land before the CTA may exit.
@@ -689,6 +702,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// 3-D view {64, rows, K/64} of a row-major [rows, K] bf16 matrix (K % 64 == 0), so
+// that one box {64, box_rows, 2} is a 128-K slab laid out as two 64-K halves.
+bool make_map_kslab(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, K / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
@@ -781,10 +809,15 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   if (A.cols == 0) return cudaErrorInvalidValue;
 
   CUtensorMap ta, tb, te;
+  // K % 64 == 0: one 3-D load per stage for B; otherwise two 2-D loads, whose out-of-range
+  // part past K is zero-filled (a 3-D view would read the next row there).
+  p.b3d = (A.cols % 64 == 0) ? 1 : 0;
+  const bool b_ok = p.b3d ? make_map_kslab(&tb, B, A.cols, rowsB, ldb * 2, kSpBN / 2)
+                          : make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64,
+                                        kSpBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 64, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64, kSpBN / 2,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !b_ok ||
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
