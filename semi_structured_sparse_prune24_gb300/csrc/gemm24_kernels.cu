@@ -157,8 +157,9 @@ struct SpmmSmem {
 // gaps after the two accumulator buffers ([BN, 256) and [256 + BN, 512)).
 template <int BN>
 __device__ __forceinline__ uint32_t meta_col(int s, int j) {
-  constexpr int kGap = (256 - BN) / 8;  // slots per gap
   const int k = 4 * s + j;
+  if constexpr (BN > 192) return 256 + 8 * k;  // one accumulator buffer: slots fill [256, 512)
+  constexpr int kGap = (256 - BN) / 8;  // slots per gap
   return k < kGap ? BN + 8 * k : 256 + BN + 8 * (k - kGap);
 }
 
@@ -212,7 +213,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                 const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
   using L = SpmmSmem<BN, STAGES>;
   constexpr int kAccCols = 256;  // accumulator buffer b starts at column 256 * b
-  static_assert(BN <= 256 && BN % 16 == 0 && 4 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
+  // BN <= 192: two accumulator buffers (the epilogue of a tile overlaps the next
+  // tile's main loop), metadata slots in the two gaps; BN > 192: one buffer.
+  constexpr int kAccBufs = BN > 192 ? 1 : 2;
+  static_assert(BN <= 256 && BN % 16 == 0, "tile width");
+  static_assert(kAccBufs == 1 ? 256 + 8 * 4 * STAGES <= 512 : 4 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
   constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, false);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -316,8 +321,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       uint32_t it = 0, tl = 0;
       bool ok = true;
       for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
-        const int b = tl & 1;
-        const uint32_t aph = (tl >> 1) & 1;
+        const int b = kAccBufs == 2 ? (tl & 1) : 0;
+        const uint32_t aph = kAccBufs == 2 ? ((tl >> 1) & 1) : (tl & 1);
         if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * kAccCols;
@@ -409,8 +414,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
       ta = 2 * ta + rank;
-      const int b = tl & 1;
-      const uint32_t aph = (tl >> 1) & 1;
+      const int b = kAccBufs == 2 ? (tl & 1) : 0;
+      const uint32_t aph = kAccBufs == 2 ? ((tl >> 1) & 1) : (tl & 1);
       if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t acc = tmem + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
@@ -761,7 +766,7 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-constexpr int kSpBN = 192;
+constexpr int kSpBN = 256;
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 4;
 
