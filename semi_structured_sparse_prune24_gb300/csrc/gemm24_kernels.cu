@@ -766,15 +766,20 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-constexpr int kSpBN = 256;
+// Sparse tile widths: N = 256 (one TMEM accumulator, the most MMA work buffered
+// per shared-memory byte) when the epilogue only stores; N = 192 with two
+// accumulators when the epilogue also reads global memory (ReLU' gate) or prunes
+// activations, so that its longer epilogue overlaps the next tile's main loop.
+constexpr int kSpBNWide = 256;
+constexpr int kSpBNOverlap = 192;
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 4;
 
-template <bool kTrans>
+template <int BN, bool kTrans>
 cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const SpmmParams& p,
                      cudaStream_t s) {
-  using L = SpmmSmem<kSpBN, kSpStages>;
-  auto kern = spmm_kernel<kSpBN, kSpStages, kTrans>;
+  using L = SpmmSmem<BN, kSpStages>;
+  auto kern = spmm_kernel<BN, kSpStages, kTrans>;
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -791,12 +796,14 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
 cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out, int64_t ldo,
                         bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s) {
   if (A.rows == 0 || rowsB == 0) return cudaSuccess;
+  const bool heavy_epilogue = epi.gate != nullptr || epi.act24.vals != nullptr;
+  const int BN = heavy_epilogue ? kSpBNOverlap : kSpBNWide;
   SpmmParams p{};
   p.rowsA = static_cast<int>(A.rows);
   p.rowsB = static_cast<int>(rowsB);
   p.K = static_cast<int>(A.cols);
   p.tilesA = static_cast<int>((A.rows + 2 * kBM - 1) / (2 * kBM));  // A tile pairs (one per cluster)
-  p.tilesB = static_cast<int>((rowsB + kSpBN - 1) / kSpBN);
+  p.tilesB = static_cast<int>((rowsB + BN - 1) / BN);
   p.num_tiles = p.tilesA * p.tilesB;
   p.group = std::min(p.tilesA, 8);
   p.nkb = static_cast<int>((A.cols + 127) / 128);
@@ -817,16 +824,19 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   // K % 64 == 0: one 3-D load per stage for B; otherwise two 2-D loads, whose out-of-range
   // part past K is zero-filled (a 3-D view would read the next row there).
   p.b3d = (A.cols % 64 == 0) ? 1 : 0;
-  const bool b_ok = p.b3d ? make_map_kslab(&tb, B, A.cols, rowsB, ldb * 2, kSpBN / 2)
+  const bool b_ok = p.b3d ? make_map_kslab(&tb, B, A.cols, rowsB, ldb * 2, BN / 2)
                           : make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, A.cols, rowsB, ldb * 2, 64,
-                                        kSpBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+                                        BN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 64, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !b_ok ||
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  return transposed_out ? run_spmm<true>(ta, tb, te, p, s) : run_spmm<false>(ta, tb, te, p, s);
+  if (heavy_epilogue)
+    return transposed_out ? run_spmm<kSpBNOverlap, true>(ta, tb, te, p, s)
+                          : run_spmm<kSpBNOverlap, false>(ta, tb, te, p, s);
+  return transposed_out ? run_spmm<kSpBNWide, true>(ta, tb, te, p, s) : run_spmm<kSpBNWide, false>(ta, tb, te, p, s);
 }
 
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
