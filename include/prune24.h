@@ -286,6 +286,15 @@ uint64_t p24_launch_count(void);
  */
 int p24_query_status(void* stream);
 
+/*
+ * p24_selftest_timeout -- exercise the failure path of the bounded waits: one
+ * kernel waits up to limit_ns (0 < limit_ns <= 1e10) on a barrier that nothing
+ * arrives on, records P24_ETIMEOUT in the device status word and returns
+ * normally. A following p24_query_status(stream) returns P24_ETIMEOUT (and
+ * clears it); the context stays usable. Nothing is faulted, trapped or hung.
+ */
+int p24_selftest_timeout(int64_t limit_ns, void* stream);
+
 /* Static text for a p24_status code. */
 const char* p24_strerror(int code);
 

@@ -7,10 +7,10 @@ and strides. There is no CPU fallback.
 """
 from ._native import (P24_EPI_ACT24, P24_EPI_BIAS, P24_EPI_RELU, P24_STEP_ACT24, P24Error, Sparse24,
                       STEP_PHASE_NAMES, STEP_PHASES, ffn24_step, ffn24_workspace_size, p24_launch_count, ld_meta, ld_vals, lib, masked_dw_gemm, p24_colsum,
-                      p24_query_status, prune24_compress, prune24_compress_both, prune24_transpose_repack,
+                      p24_query_status, p24_selftest_timeout, prune24_compress, prune24_compress_both, prune24_transpose_repack,
                       spmm24_bwd_dx, spmm24_fwd, spmm24_fwd_sparse_act)
 
 __all__ = ["STEP_PHASES", "STEP_PHASE_NAMES", "p24_launch_count", "P24Error", "Sparse24", "ffn24_step", "ffn24_workspace_size", "ld_meta", "ld_vals", "lib",
-           "masked_dw_gemm", "p24_colsum", "p24_query_status", "prune24_compress", "prune24_compress_both",
+           "masked_dw_gemm", "p24_colsum", "p24_query_status", "p24_selftest_timeout", "prune24_compress", "prune24_compress_both",
            "prune24_transpose_repack", "spmm24_bwd_dx", "spmm24_fwd", "spmm24_fwd_sparse_act",
            "P24_EPI_ACT24", "P24_EPI_BIAS", "P24_EPI_RELU", "P24_STEP_ACT24"]

@@ -65,6 +65,7 @@ def _load() -> C.CDLL:
         "ffn24_step_traced": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp, C.POINTER(vp), i32]),
         "p24_launch_count": (C.c_uint64, []),
         "p24_query_status": (i32, [vp]),
+        "p24_selftest_timeout": (i32, [i64, vp]),
         "p24_strerror": (C.c_char_p, [i32]),
     }
     for name, (res, args) in sigs.items():
@@ -313,6 +314,11 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
 
 def p24_launch_count() -> int:
     return int(lib.p24_launch_count())
+
+
+def p24_selftest_timeout(limit_ns: int = 10_000_000, stream=None) -> None:
+    """Launch the bounded-wait failure self test (see include/prune24.h)."""
+    _check(lib.p24_selftest_timeout(limit_ns, _stream(stream)), "p24_selftest_timeout")
 
 
 def p24_query_status(stream=None) -> int:

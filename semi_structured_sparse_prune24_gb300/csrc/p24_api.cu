@@ -350,6 +350,13 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   return P24_OK;
 }
 
+int p24_selftest_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 10000000000LL) return P24_EINVAL;
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_selftest_timeout(static_cast<uint64_t>(limit_ns), st, as_stream(stream)));
+}
+
 int p24_query_status(void* stream) {
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return P24_ECUDA;
   int v = 0;

@@ -17,6 +17,7 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
 cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s);
 cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s);
 int64_t colsum_slabs(int64_t M);
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s);
 // Same sums with the library's fixed device scratch instead of a caller workspace.
 constexpr int64_t kNoAllocColsumScratch = int64_t(1) << 20;  // floats (4 MiB per GPU)

@@ -73,6 +73,19 @@ __device__ __forceinline__ bool p24_wait(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait with a limit chosen at run time; on expiry records P24_ETIMEOUT.
+__device__ __forceinline__ bool p24_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns, int* status) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) {
+      atomicExch(status, -4 /* P24_ETIMEOUT */);
+      return false;
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag and records nothing: used on the
 // way out of a kernel, to let copies and MMAs already issued finish.
 __device__ __forceinline__ bool p24_wait_quiet(uint64_t* bar, uint32_t parity) {

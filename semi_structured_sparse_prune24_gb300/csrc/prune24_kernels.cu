@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "p24_internal.h"
+#include "p24_ptx.cuh"
 
 namespace p24 {
 namespace {
@@ -301,9 +302,26 @@ __global__ void colsum_final_kernel(const float* __restrict__ part, int64_t S, i
 // exits. All calls share it (calls that overlap on the GPU race on it).
 __device__ __align__(256) float g_colsum_scratch[kNoAllocColsumScratch];
 
+// Failure-path self test: one thread waits on an mbarrier that nothing ever
+// arrives on. The bounded wait expires after limit_ns, records P24_ETIMEOUT in the
+// status word and the kernel returns normally (no trap, no hang).
+__global__ void selftest_timeout_kernel(uint64_t limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  p24_wait_for(&bar, 0, limit_ns, status);
+}
+
 inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n < 1 ? 1 : n) : 65535); }
 
 }  // namespace
+
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
+  selftest_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s) {
   const int64_t per_row = (d.ldv - d.cols / 2) + (d.ldm - (d.cols / 4 + 1) / 2);
