@@ -167,10 +167,16 @@ int spmm24_fwd_sparse_act(const p24_sparse* Xs, const void* Wm, int64_t N,
  *   gate  : optional device bf16 [M, ldg] (the forward ReLU output); where
  *           gate <= 0 the gradient is 0 (ReLU'(0) = 0). NULL = no gate.
  *   dX    : device bf16 [M, lddx], K columns.
+ *   dbias : optional device fp32 [K], 16-byte aligned: receives the bias
+ *           gradient of the layer below, dbias[k] = sum over m of dX[m, k]
+ *           (the stored bf16 values), fused into the GEMM's epilogue. It is
+ *           zeroed on `stream` and then accumulated with fp32 atomics, so the
+ *           summation order (and the last bits) may differ from run to run;
+ *           p24_colsum gives a fixed-order sum. NULL = not computed.
  */
 int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT,
                   const void* gate, int64_t ldg, void* dX, int64_t lddx,
-                  void* stream);
+                  float* dbias, void* stream);
 
 /*
  * masked_dw_gemm -- weight gradient of a 2:4 linear, kept on the forward mask:
@@ -232,6 +238,8 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
  *   H  = ReLU(X W_up^T + b_up)           (ACT24: H pruned 2:4 along ffn)
  *   Y  = H W_down^T + b_down
  *   dH = (dY W_down_bwd) * [H > 0];  db_up = colsum(dH);  db_down = colsum(dY)
+ *   (db_up is fused into the dH epilogue with fp32 atomics, so its last bits may
+ *   vary from run to run; db_down is a fixed-order sum)
  *   dW_down = (dY^T H) on mask(W_down);  dX = dH W_up_bwd;  dW_up = (dH^T X) on mask(W_up)
  * All tensors are dense, row-major, contiguous (row stride = column count):
  *   X, dY, Y, dX : bf16 [M, d];  W_up, dW_up : bf16 [ffn, d];
@@ -268,7 +276,7 @@ int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* st
  * per-kernel timing without a synchronisation: events[2p] before and
  * events[2p+1] after phase p, for p < min(P24_STEP_PHASES, n_events / 2).
  * Phases: 0 prune+double-prune W_up, 1 the same for W_down, 2 up forward (H),
- * 3 down forward (Y), 4 down backward dX (dH), 5 bias gradients, 6 dW_down,
+ * 3 down forward (Y), 4 down backward dX (dH and db_up), 5 db_down, 6 dW_down,
  * 7 up backward dX, 8 dW_up. events may be NULL (then identical to ffn24_step).
  */
 #define P24_STEP_PHASES 9

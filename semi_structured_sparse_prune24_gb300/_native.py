@@ -55,7 +55,7 @@ def _load() -> C.CDLL:
         "prune24_compress_both": (i32, [vp, i64, i64, i64, sp, sp, vp, i64, vp]),
         "spmm24_fwd": (i32, [vp, i64, i64, sp, vp, u32, vp, i64, sp, vp]),
         "spmm24_fwd_sparse_act": (i32, [sp, vp, i64, i64, vp, u32, vp, i64, vp]),
-        "spmm24_bwd_dx": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, vp]),
+        "spmm24_bwd_dx": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, vp, vp]),
         "masked_dw_gemm": (i32, [vp, i64, vp, i64, i64, sp, vp, i64, vp]),
         "p24_colsum_workspace_size": (sz, [i64, i64]),
         "p24_colsum": (i32, [vp, i64, i64, i64, vp, vp, sz, vp]),
@@ -218,7 +218,8 @@ def spmm24_fwd_sparse_act(Xs: Sparse24, Wm: torch.Tensor, bias: torch.Tensor | N
 
 
 def spmm24_bwd_dx(dY: torch.Tensor, WbwdT: Sparse24, gate: torch.Tensor | None = None,
-                  dX: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                  dX: torch.Tensor | None = None, dbias: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dX = (dY W_bwd) * [gate > 0]; with dbias (fp32 [K]) also its column sums, fused."""
     M, N, lddy = _mat(dY, name="dY")
     K = WbwdT.rows
     dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device) if dX is None else dX
@@ -227,8 +228,10 @@ def spmm24_bwd_dx(dY: torch.Tensor, WbwdT: Sparse24, gate: torch.Tensor | None =
     if gate is not None:
         _, _, ldg = _mat(gate, name="gate")
     w = WbwdT.c()
+    if dbias is not None and (dbias.dtype != torch.float32 or dbias.numel() != K or not dbias.is_contiguous()):
+        raise ValueError(f"dbias must be a contiguous fp32 tensor of {K} elements")
     _check(lib.spmm24_bwd_dx(dY.data_ptr(), M, lddy, C.byref(w), _ptr(gate), ldg, dX.data_ptr(), lddx,
-                             _stream(stream)), "spmm24_bwd_dx")
+                             _ptr(dbias), _stream(stream)), "spmm24_bwd_dx")
     return dX
 
 
@@ -271,7 +274,7 @@ def ffn24_workspace_size(M: int, d: int, ffn: int, act24: bool = False) -> int:
 
 
 STEP_PHASES = 9
-STEP_PHASE_NAMES = ("prune_up", "prune_down", "up_fwd", "down_fwd", "down_bwd_dx", "bias_grads", "dW_down",
+STEP_PHASE_NAMES = ("prune_up", "prune_down", "up_fwd", "down_fwd", "down_bwd_dx", "db_down", "dW_down",
                     "up_bwd_dx", "dW_up")
 
 

@@ -58,6 +58,7 @@ struct SpmmParams {
   int relu;
   const uint16_t* gate;
   int64_t ldg;
+  float* dbias;              // += column sums (over B rows) of the stored output, per A row
   uint16_t* a24_vals;
   int64_t a24_ldv;
   uint8_t* a24_meta;
@@ -93,6 +94,22 @@ __device__ __forceinline__ uint32_t bf16_pos_mask(uint32_t w) {
   const uint32_t lo = ((w & 0x8000u) == 0 && (w & 0x7FFFu) != 0) ? 0x0000FFFFu : 0u;
   const uint32_t hi = ((w & 0x80000000u) == 0 && (w & 0x7FFF0000u) != 0) ? 0xFFFF0000u : 0u;
   return lo | hi;
+}
+
+// One byte of gate bits -> masks for the four bf16 pairs of a 16-byte piece.
+__device__ __forceinline__ uint32_t pair_mask(uint32_t byte, int i) {
+  return (((byte >> (2 * i)) & 1u) ? 0x0000FFFFu : 0u) | (((byte >> (2 * i + 1)) & 1u) ? 0xFFFF0000u : 0u);
+}
+// Bit i set where bf16 value i of the piece is > 0.
+__device__ __forceinline__ uint32_t positive_bits(const uint4& x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t b = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t m = bf16_pos_mask(w[i]);
+    b |= ((m & 1u) << (2 * i)) | (((m >> 16) & 1u) << (2 * i + 1));
+  }
+  return b;
 }
 
 // 2:4 pick on a group held as two words (see prune24_kernels.cu for the key).
@@ -148,7 +165,8 @@ struct SpmmSmem {
   static constexpr int kOffB = kOffA + STAGES * kA;
   static constexpr int kOffE = kOffB + STAGES * kB;
   static constexpr int kOffStage = kOffE + kEBufs * kE;  // epilogue transpose, 4 warps x 32x32 bf16
-  static constexpr int kOffBar = kOffStage + 4 * 32 * 32 * 2;
+  static constexpr int kOffGate = kOffStage + 4 * 32 * 32 * 2;  // gate words: 4 warps x BN tokens x 32 features
+  static constexpr int kOffBar = kOffGate + 4 * BN * 4;
   static constexpr int kBytes = kOffBar + 8 * (3 * STAGES + 2 * kEBufs + 5) + 16;
   static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
 };
@@ -207,7 +225,14 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask)
       : "memory");
 }
 
-template <int BN, int STAGES, bool kTransOut>
+// Epilogue kinds, fixed at compile time so that the store loops carry no branches
+// for features a call does not use.
+enum SpmmEpi : int {
+  kEpiStore = 0,  // bias and ReLU only
+  kEpiFull = 1,   // any of: ReLU' gate, 2:4 activation prune, column sums (transposed output)
+};
+
+template <int BN, int STAGES, bool kTransOut, int kEpi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
@@ -409,6 +434,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
     const int q = warp & 3;
     uint16_t* stage = reinterpret_cast<uint16_t*>(smem + L::kOffStage) + q * 32 * 32;
+    // ReLU' gate of this warp's 32 features: one 32-bit word per token of the tile
+    uint32_t* gstage = reinterpret_cast<uint32_t*>(smem + L::kOffGate) + q * BN;
     uint32_t tl = 0;
     for (int t = cid; t < p.num_tiles; t += ncl, ++tl) {
       int ta, tb;
@@ -416,6 +443,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       ta = 2 * ta + rank;
       const int b = kAccBufs == 2 ? (tl & 1) : 0;
       const uint32_t aph = kAccBufs == 2 ? ((tl >> 1) & 1) : (tl & 1);
+      // Transposed output: in the store phase lane l handles token j = 8r + l / 4 of
+      // each chunk and features n_piece .. n_piece + 7 of the tile.
+      const int n_warp = ta * kBM + q * 32;
+      const int n_piece = n_warp + (lane & 3) * 8;
+      if (kTransOut && kEpi == kEpiFull && p.gate) {
+        // The ReLU' gate of this warp's 32 features, one word per token (bit l:
+        // gate(m, n_warp + l) > 0), read from the bf16 gate while the tile's main
+        // loop still runs, so that no load sits in the epilogue's critical path.
+        for (int j = lane; j < BN; j += 32) {
+          const int m = tb * BN + j;
+          uint32_t word = 0;
+          if (m < p.rowsB) {
+            const uint16_t* g = p.gate + static_cast<int64_t>(m) * p.ldg + n_warp;
+            uint4 x[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              x[k] = n_warp + 8 * k < p.rowsA ? *reinterpret_cast<const uint4*>(g + 8 * k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) word |= positive_bits(x[k]) << (8 * k);
+          }
+          gstage[j] = word;
+        }
+        __syncwarp();
+      }
+      float dsum[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dsum[i] = 0.f;
       if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t acc = tmem + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
@@ -438,17 +492,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int j = r * 8 + (lane >> 2);
-            const int piece = lane & 3;
             const int m = tb * BN + c * 32 + j;
-            const int n = ta * kBM + q * 32 + piece * 8;
-            uint4 x = *reinterpret_cast<const uint4*>(stage + j * 32 + piece * 8);
-            if (m < p.rowsB && n < p.rowsA) {
+            const int n = n_piece;
+            uint4 x = *reinterpret_cast<const uint4*>(stage + j * 32 + (lane & 3) * 8);
+            const bool valid = m < p.rowsB && n < p.rowsA;
+            if (valid && kEpi != kEpiFull) {
+              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
+            } else if (valid) {
               if (p.gate) {
-                const uint4 g = *reinterpret_cast<const uint4*>(p.gate + static_cast<int64_t>(m) * p.ldg + n);
-                x.x &= bf16_pos_mask(g.x);
-                x.y &= bf16_pos_mask(g.y);
-                x.z &= bf16_pos_mask(g.z);
-                x.w &= bf16_pos_mask(g.w);
+                const uint32_t gb = (gstage[c * 32 + j] >> (8 * (lane & 3))) & 0xFFu;
+                x.x &= pair_mask(gb, 0);
+                x.y &= pair_mask(gb, 1);
+                x.z &= pair_mask(gb, 2);
+                x.w &= pair_mask(gb, 3);
               }
               if (p.a24_vals) {
                 const uint32_t n0 = pick2_nibble(x.x, x.y);
@@ -460,6 +516,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                 *reinterpret_cast<uint2*>(p.a24_vals + static_cast<int64_t>(m) * p.a24_ldv + n / 2) =
                     make_uint2(k0, k1);
                 p.a24_meta[static_cast<int64_t>(m) * p.a24_ldm + n / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
+              }
+              if (p.dbias) {
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  dsum[2 * i] += __uint_as_float(xw[i] << 16);
+                  dsum[2 * i + 1] += __uint_as_float(xw[i] & 0xFFFF0000u);
+                }
               }
               *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
             }
@@ -500,6 +564,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
+      if (kTransOut && kEpi == kEpiFull && p.dbias) {
+        // lanes l, l ^ 4, ..., l ^ 28 hold the same 8 features: sum them, then one
+        // fp32 atomic per feature and tile
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          dsum[i] += __shfl_xor_sync(0xffffffffu, dsum[i], 4);
+          dsum[i] += __shfl_xor_sync(0xffffffffu, dsum[i], 8);
+          dsum[i] += __shfl_xor_sync(0xffffffffu, dsum[i], 16);
+        }
+        if (lane < 4) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (n_piece + i < p.rowsA) atomicAdd(p.dbias + n_piece + i, dsum[i]);
+        }
+      }
     }
   }
 
@@ -767,19 +846,20 @@ int num_sms() {
 }
 
 // Sparse tile widths: N = 256 (one TMEM accumulator, the most MMA work buffered
-// per shared-memory byte) when the epilogue only stores; N = 192 with two
-// accumulators when the epilogue also reads global memory (ReLU' gate) or prunes
-// activations, so that its longer epilogue overlaps the next tile's main loop.
+// per shared-memory byte) unless the epilogue prunes activations; that one takes
+// N = 192 with two accumulators, so that its longer epilogue overlaps the next
+// tile's main loop. The ReLU' gate stays on N = 256: the epilogue turns it into
+// bits while the tile's main loop runs, before the accumulator is ready.
 constexpr int kSpBNWide = 256;
 constexpr int kSpBNOverlap = 192;
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 4;
 
-template <int BN, bool kTrans>
+template <int BN, bool kTrans, int kEpi>
 cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const SpmmParams& p,
                      cudaStream_t s) {
   using L = SpmmSmem<BN, kSpStages>;
-  auto kern = spmm_kernel<BN, kSpStages, kTrans>;
+  auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi>;
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -796,7 +876,7 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
 cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out, int64_t ldo,
                         bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s) {
   if (A.rows == 0 || rowsB == 0) return cudaSuccess;
-  const bool heavy_epilogue = epi.gate != nullptr || epi.act24.vals != nullptr;
+  const bool heavy_epilogue = epi.act24.vals != nullptr;
   const int BN = heavy_epilogue ? kSpBNOverlap : kSpBNWide;
   SpmmParams p{};
   p.rowsA = static_cast<int>(A.rows);
@@ -813,6 +893,8 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   p.relu = epi.relu ? 1 : 0;
   p.gate = static_cast<const uint16_t*>(epi.gate);
   p.ldg = epi.ldg;
+  p.dbias = epi.dbias;
+  if (!transposed_out && (epi.gate || epi.dbias)) return cudaErrorInvalidValue;
   p.a24_vals = static_cast<uint16_t*>(epi.act24.vals);
   p.a24_ldv = epi.act24.ldv;
   p.a24_meta = epi.act24.meta;
@@ -833,10 +915,13 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (heavy_epilogue)
-    return transposed_out ? run_spmm<kSpBNOverlap, true>(ta, tb, te, p, s)
-                          : run_spmm<kSpBNOverlap, false>(ta, tb, te, p, s);
-  return transposed_out ? run_spmm<kSpBNWide, true>(ta, tb, te, p, s) : run_spmm<kSpBNWide, false>(ta, tb, te, p, s);
+  if (!transposed_out) {
+    if (heavy_epilogue) return cudaErrorInvalidValue;  // the activation prune is transposed-only
+    return run_spmm<kSpBNWide, false, kEpiStore>(ta, tb, te, p, s);
+  }
+  if (heavy_epilogue) return run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, p, s);
+  if (epi.gate || epi.dbias) return run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, p, s);
+  return run_spmm<kSpBNWide, true, kEpiStore>(ta, tb, te, p, s);
 }
 
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,

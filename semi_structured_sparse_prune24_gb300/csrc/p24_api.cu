@@ -186,18 +186,22 @@ int spmm24_fwd_sparse_act(const p24_sparse* Xs, const void* Wm, int64_t N, int64
 }
 
 int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT, const void* gate, int64_t ldg,
-                  void* dX, int64_t lddx, void* stream) {
+                  void* dX, int64_t lddx, float* dbias, void* stream) {
   P24_TRY(check_sparse(WbwdT));
   const int64_t K = WbwdT->rows, N = WbwdT->cols;
   if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
   P24_TRY(check_dense(dY, M, N, lddy));
   P24_TRY(check_dense(dX, M, K, lddx));
   if (gate) P24_TRY(check_dense(gate, M, K, ldg));
-  if (M == 0 || K == 0) return P24_OK;
+  if (dbias && !aligned16(dbias)) return P24_EALIGN;
+  if (K == 0) return P24_OK;
+  if (dbias) P24_TRY(cuda_status(cudaMemsetAsync(dbias, 0, K * 4, as_stream(stream))));
+  if (M == 0) return P24_OK;
   if (N == 0) return P24_EUNSUPPORTED;
   EpiArgs epi;
   epi.gate = gate;
   epi.ldg = ldg;
+  epi.dbias = dbias;
   int* st = device_status_ptr();
   if (!st) return P24_ECUDA;
   return cuda_status(launch_spmm(*WbwdT, dY, M, lddy, dX, lddx, /*transposed_out=*/true, epi, st, as_stream(stream)));
@@ -327,14 +331,17 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
     P24_PHASE(3, P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s))));
   else
     P24_PHASE(3, P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s))));
-  // 4. dH = (dY W_down_bwd) * [H > 0]
+  // 4. dH = (dY W_down_bwd) * [H > 0], with db_up = column sums of dH fused into its epilogue
   EpiArgs g;
   g.gate = a->H;
   g.ldg = ffn;
-  P24_PHASE(4, P24_TRY(cuda_status(launch_spmm(L.dn_bwdT, a->dY, M, d, dHv, ffn, true, g, st, s))));
-  // 5. bias gradients
+  g.dbias = a->db_up;
+  P24_PHASE(4, {
+    if (a->db_up) P24_TRY(cuda_status(cudaMemsetAsync(a->db_up, 0, ffn * 4, s)));
+    P24_TRY(cuda_status(launch_spmm(L.dn_bwdT, a->dY, M, d, dHv, ffn, true, g, st, s)));
+  });
+  // 5. db_down = column sums of dY
   P24_PHASE(5, {
-    if (a->db_up) P24_TRY(cuda_status(launch_colsum(dHv, M, ffn, ffn, a->db_up, cs, s)));
     if (a->db_down) P24_TRY(cuda_status(launch_colsum(a->dY, M, d, d, a->db_down, cs, s)));
   });
   // 6. dW_down = (dY^T H) on mask(W_down)

@@ -29,6 +29,7 @@ struct EpiArgs {
   bool relu = false;
   const void* gate = nullptr;   // bf16 [M, ldg] ReLU output for the backward gate, or null
   int64_t ldg = 0;
+  float* dbias = nullptr;              // += column sums of the stored output (transposed output only)
   p24_sparse act24{};           // compressed activation output (vals != null => enabled)
 };
 

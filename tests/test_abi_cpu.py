@@ -82,7 +82,9 @@ def test_host_validation_rejects_before_launch(native):
     assert L.spmm24_fwd(fake, 8, 16, C.byref(w), None, native.P24_EPI_BIAS, fake, 16, None, None) == EINVAL
     w12 = _sp(fake, fake, 16, 12, 8, 16, native)
     assert L.spmm24_fwd(fake, 8, 16, C.byref(w12), None, 0, fake, 16, None, None) == EINVAL
-    assert L.spmm24_bwd_dx(None, 8, 16, C.byref(w), None, 0, fake, 16, None) == EINVAL
+    assert L.spmm24_bwd_dx(None, 8, 16, C.byref(w), None, 0, fake, 16, None, None) == EINVAL
+    # fused bias gradient must be 16-byte aligned
+    assert L.spmm24_bwd_dx(fake, 8, 16, C.byref(w), None, 0, fake, 16, fake + 4, None) == native.P24_EALIGN
     assert L.masked_dw_gemm(fake, 16, fake, 16, 8, None, fake, 16, None) == EINVAL
     # colsum workspace too small
     assert L.p24_colsum(fake, 100, 16, 16, fake, fake, 8, None) == native.P24_ENOSPACE

@@ -8,7 +8,7 @@ import torch
 from oracle import prune24_oracle as O
 from synth24 import normal_bf16, normal_f32
 from tests.conftest import bits_of
-from tests.p24_testutil import assert_bits_equal, assert_close, sparse_bits
+from tests.p24_testutil import assert_bits_equal, assert_close, sparse_bits, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -71,11 +71,30 @@ def test_spmm24_bwd_dx(P, M, N, K, gated):
     dY = normal_bf16((M, N), 1.0, 3, 6, "cuda")
     fwd, bwdT = P.prune24_compress_both(W)
     gate = torch.relu(normal_bf16((M, K), 1.0, 3, 7, "cuda")) if gated else None
-    dX = P.spmm24_bwd_dx(dY, bwdT, gate=gate)
+    dbias = torch.full((K,), 7.0, dtype=torch.float32, device="cuda")   # overwritten, not accumulated into
+    dX = P.spmm24_bwd_dx(dY, bwdT, gate=gate, dbias=dbias)
     torch.cuda.synchronize()
     tv, tm = sparse_bits(bwdT)
-    ref, _ = O.spmm24_bwd_dx(bits_of(dY), tv, tm, N, gate=None if gate is None else bits_of(gate))
+    ref, ref_b = O.spmm24_bwd_dx(bits_of(dY), tv, tm, N, gate=None if gate is None else bits_of(gate))
     assert_close(dX, ref, "dX")
+    # fused bias gradient: the column sums of the stored bf16 dX (fp32 atomics, any order) ...
+    g = O.bf16_to_f32(bits_of(dX)).astype(np.float64)
+    db = dbias.cpu().numpy().astype(np.float64)
+    # recursive fp32 summation: |error| <= (additions on the longest path) * 2^-24 * sum |x|;
+    # a lane adds <= 32 values, 8 lanes are combined in 3 steps, then one atomic per tile
+    fp32_bound = (32 + 3 + M / 128 + 2) * 2.0 ** -24 * np.abs(g).sum(0) + 1e-30
+    assert np.all(np.abs(db - g.sum(0)) <= fp32_bound), np.abs(db - g.sum(0)).max()
+    # ... and against the oracle's column sums, within the propagated bf16 rounding of dX
+    assert_close(dbias, O.colsum(ref_b), "dbias", 4 * np.sqrt((ulp_bf16(ref_b) ** 2).sum(0)))
+
+
+def test_spmm24_bwd_dx_empty_tokens_zeroes_dbias(P):
+    W = normal_bf16((64, 128), 0.02, 3, 2, "cuda")
+    _, bwdT = P.prune24_compress_both(W)
+    dbias = torch.full((128,), 3.0, dtype=torch.float32, device="cuda")
+    P.spmm24_bwd_dx(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), bwdT, dbias=dbias)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dbias).item() == 0
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 128, 256), (520, 392, 1032), (1000, 264, 8200)])
