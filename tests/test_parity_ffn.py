@@ -16,7 +16,7 @@ import torch
 from oracle import prune24_oracle as O
 from synth24 import WORKLOADS, FFNWorkload, ffn_inputs
 from tests.conftest import bits_of
-from tests.p24_testutil import assert_close, propagated, ulp_bf16
+from tests.p24_testutil import assert_bits_equal, assert_close, propagated, sparse_bits, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -34,9 +34,11 @@ def run_gpu(P, inp, act24):
     return o
 
 
-def act_flip_groups(Hg_bits, ref, ffn):
+def act_flip_groups(Hg_bits, ref, ffn, scale):
     """[M, ffn/4] bool: activation groups whose GPU 2:4 pick differs from the oracle's.
-    Each must be a near-tie: the two picks keep magnitudes equal up to bf16 rounding."""
+    Each must be a near-tie: the two picks keep magnitudes equal up to bf16 rounding,
+    or differ by a value within rounding of 0 (a ReLU-gate decision on a pre-activation
+    near 0, judged like the gate flips below: at most 1e-3 * rms(H))."""
     mg = O.mask_from_meta(O.compress24(Hg_bits)[1], ffn)
     mr = O.mask_from_meta(ref["Hs_meta"], ffn)
     diff = (mg != mr).reshape(mg.shape[0], -1, 4).any(-1)
@@ -44,7 +46,7 @@ def act_flip_groups(Hg_bits, ref, ffn):
         h = np.abs(ref["H_ref"][m, 4 * g:4 * g + 4])
         kept_r = h[mr[m, 4 * g:4 * g + 4]]
         kept_g = h[mg[m, 4 * g:4 * g + 4]]
-        assert np.allclose(np.sort(kept_r), np.sort(kept_g), rtol=2 ** -7, atol=1e-6), (m, g, h)
+        assert np.allclose(np.sort(kept_r), np.sort(kept_g), rtol=2 ** -7, atol=1e-3 * scale), (m, g, h)
     return diff
 
 
@@ -58,11 +60,11 @@ def disputed_positions(o, ref, w: FFNWorkload, act24: bool):
     Hg = O.bf16_to_f32(bits_of(o["H"]))
     Hr = O.bf16_to_f32(ref["H_used"])
     disputed = np.zeros(Hg.shape, dtype=bool)
+    scale = float(np.sqrt(np.mean(ref["H_ref"].astype(np.float64) ** 2))) or 1.0
     if act24:
-        groups = act_flip_groups(bits_of(o["H"]), ref, w.ffn)
+        groups = act_flip_groups(bits_of(o["H"]), ref, w.ffn, scale)
         disputed |= np.repeat(groups, 4, axis=1)
     gate = ((Hg > 0) != (Hr > 0)) & ~disputed
-    scale = float(np.sqrt(np.mean(ref["H_ref"].astype(np.float64) ** 2))) or 1.0
     near_zero = np.maximum(Hg, Hr)[gate]
     assert np.all(near_zero <= 1e-3 * scale), (near_zero.max(), scale)
     disputed |= gate
@@ -137,7 +139,7 @@ def test_ffn_step_integer_inputs_bit_exact(P, shape, act24):
     ref = oracle_step(inp, act24)
     # every fp32 sum stays far below 2**24, so the exact result is order-independent
     assert np.abs(ref["dW_up_ref"]).max() < 2 ** 20 and np.abs(ref["dW_down_ref"]).max() < 2 ** 20
-    from tests.p24_testutil import assert_bits_equal
+
     assert_bits_equal(bits_of(o["H"]), ref["H_used"] if act24 else ref["H"], "H")
     assert_bits_equal(bits_of(o["Y"]), ref["Y"], "Y")
     assert_bits_equal(bits_of(o["dX"]), ref["dX"], "dX")
@@ -165,59 +167,74 @@ def test_ffn_step_workloads(P, name, act24):
     compare_step(o, oracle_step(inp, act24), w, act24)
 
 
-def test_ffn_step_70b_bench_workload_sampled(P):
-    """The bench's workload (d=8192, ffn=28672, M=16384) in the bench's launch
-    configuration; 16 token rows and 16 weight rows are recomputed by the oracle."""
-    w = WORKLOADS["70b_m16384"]
+@pytest.mark.parametrize("name", ["70b_m16384", "70b_m2048", "7b_act24"])
+def test_ffn_step_large_workloads_sampled(P, name):
+    """The large configurations in the bench's launch configuration. Compressed and
+    double-pruned weights (and W_down on its mask) are checked bit-exactly in full.
+    Outputs are checked on 512 seeded token rows (H, Y, dX), 512 hidden units
+    (dW_up, db_up) and 512 model features (dW_down, db_down), recomputed by the oracle
+    from the seeded inputs alone; the oracle's full H decides which positions carry
+    a legitimately different rounded decision (see disputed_positions)."""
+    w = WORKLOADS[name]
+    act24 = w.act24
     inp = ffn_inputs(w, seed=0, device="cuda", bias=False)
-    o = run_gpu(P, inp, False)
+    o = run_gpu(P, inp, act24)
     X, Wu, Wd, dY = (bits_of(inp[k]) for k in ("X", "W_up", "W_down", "dY"))
-    up_v, up_m = O.compress24(Wu)
-    dn_v, dn_m = O.compress24(Wd)
-    upT_v, upT_m = O.double_prune(up_v, up_m, w.ffn, w.d)
-    dnT_v, dnT_m = O.double_prune(dn_v, dn_m, w.d, w.ffn)
-    rng = np.random.default_rng(5)
-    ms = np.sort(rng.choice(w.M, 16, replace=False))
-    fs = np.sort(rng.choice(w.ffn, 16, replace=False))
-    ns = np.sort(rng.choice(w.d, 16, replace=False))
     tm = lambda a: torch.as_tensor(a, device="cuda")  # noqa: E731
-    def gate_flips(H_gpu, H_bits, H_ref):
-        """ReLU-gate decisions taken differently on the two sides; each must sit at a
-        pre-activation within rounding of 0 (see the module docstring)."""
-        g, r = O.bf16_to_f32(bits_of(H_gpu)), O.bf16_to_f32(H_bits)
-        flip = (g > 0) != (r > 0)
-        scale = float(np.sqrt(np.mean(H_ref.astype(np.float64) ** 2))) or 1.0
-        assert np.all(np.maximum(g, r)[flip] <= 1e-3 * scale)
-        return flip
 
-    Wd2 = O.bf16_to_f32(O.decompress24(dn_v, dn_m, w.ffn)) ** 2           # [d, ffn]
-    WubT2 = O.bf16_to_f32(O.decompress24(upT_v, upT_m, w.ffn)) ** 2       # [d, ffn]
+    # weights: fresh masks and double prunes, bit for bit in full
+    Wm = torch.empty((w.d, w.ffn), dtype=torch.bfloat16, device="cuda")
+    gu, guT = P.prune24_compress_both(inp["W_up"])
+    gd, gdT = P.prune24_compress_both(inp["W_down"], W_masked=Wm)
+    up_v, up_m = O.compress24(Wu, gu.ldv, gu.ldm)
+    dn_v, dn_m = O.compress24(Wd, gd.ldv, gd.ldm)
+    upT_v, upT_m = O.double_prune(up_v, up_m, w.ffn, w.d, guT.ldv, guT.ldm)
+    dnT_v, dnT_m = O.double_prune(dn_v, dn_m, w.d, w.ffn, gdT.ldv, gdT.ldm)
+    for g, (rv, rm), nm in ((gu, (up_v, up_m), "W_up fwd"), (guT, (upT_v, upT_m), "W_up bwdT"),
+                            (gd, (dn_v, dn_m), "W_down fwd"), (gdT, (dnT_v, dnT_m), "W_down bwdT")):
+        gv, gmeta = sparse_bits(g)
+        assert_bits_equal(gv, rv, nm + " vals")
+        assert_bits_equal(gmeta, rm, nm + " meta")
+    assert_bits_equal(bits_of(Wm), O.decompress24(dn_v, dn_m, w.ffn), "W_down on its mask")
+    del gu, guT, gd, gdT, Wm
+
+    # the oracle's full H (needed for dW_down anyway) and the disputed decisions
+    H_r, H_b = O.spmm24_fwd(X, up_v, up_m, w.d, relu=True)
+    ref = {"H_ref": H_r, "H": H_b}
+    if act24:
+        ref["Hs_vals"], ref["Hs_meta"] = O.compress24(H_b)
+        ref["H_used"] = O.decompress24(ref["Hs_vals"], ref["Hs_meta"], w.ffn)
+    else:
+        ref["H_used"] = H_b
+    Hu = ref["H_used"]
+    dm, df, _ = disputed_positions(o, ref, w, act24)
+    rng = np.random.default_rng(5)
+    ms = np.setdiff1d(np.sort(rng.choice(w.M, 512, replace=False)), dm)
+    fs = np.setdiff1d((4 * np.sort(rng.choice(w.ffn // 4, 128, replace=False))[:, None] + np.arange(4)).ravel(), df)
+    ns = np.sort(rng.choice(w.d, 512, replace=False))
+    kf_all = np.setdiff1d(np.arange(w.ffn), df)
+    assert len(ms) >= 500 and len(fs) >= 500
+
     # token rows: H, Y, dX
-    H_r, H_b = O.spmm24_fwd(X[ms], up_v, up_m, w.d, relu=True)
-    assert_close(o["H"][tm(ms)], H_r, "H rows")
-    Y_r, _ = O.spmm24_fwd(H_b, dn_v, dn_m, w.ffn)
-    assert_close(o["Y"][tm(ms)], Y_r, "Y rows", propagated(ulp_bf16(H_b) ** 2, Wd2.T))
-    _, dH_b = O.spmm24_bwd_dx(dY[ms], dnT_v, dnT_m, w.d, gate=H_b)
+    assert_close(o["H"][tm(ms)], O.bf16_to_f32(Hu[ms]) if act24 else H_r[ms], "H rows")
+    Wd2 = O.bf16_to_f32(O.decompress24(dn_v, dn_m, w.ffn)) ** 2           # [d, ffn]
+    Y_r, _ = O.spmm24_fwd(Hu[ms], dn_v, dn_m, w.ffn)
+    assert_close(o["Y"][tm(ms)], Y_r, "Y rows", propagated(ulp_bf16(Hu[ms]) ** 2, Wd2.T))
+    del Wd2
+    _, dH_b = O.spmm24_bwd_dx(dY[ms], dnT_v, dnT_m, w.d, gate=Hu[ms])
     dX_r, _ = O.spmm24_bwd_dx(dH_b, upT_v, upT_m, w.ffn)
-    keep = ~gate_flips(o["H"][tm(ms)], H_b, H_r).any(axis=1)
-    assert keep.sum() >= len(ms) - 2
-    assert_close(o["dX"][tm(ms[keep])], dX_r[keep], "dX rows",
-                 propagated(ulp_bf16(dH_b[keep]) ** 2, WubT2.T))
-    del Wd2, WubT2
-    # weight rows: dW_up[fs, :] needs dH[:, fs] over all tokens
-    Hc_r, Hc_b = O.spmm24_fwd(X, up_v[fs], up_m[fs], w.d, relu=True)        # H[:, fs]
-    _, dHc_b = O.spmm24_bwd_dx(dY, dnT_v[fs], dnT_m[fs], w.d, gate=Hc_b)     # dH[:, fs]
+    WubT2 = O.bf16_to_f32(O.decompress24(upT_v, upT_m, w.ffn)) ** 2       # [d, ffn]
+    assert_close(o["dX"][tm(ms)], dX_r, "dX rows", propagated(ulp_bf16(dH_b) ** 2, WubT2.T))
+    del WubT2
+    # hidden units: dW_up[fs, :] and db_up[fs] need dH[:, fs] over all tokens
+    _, dHc_b = O.spmm24_bwd_dx(dY, dnT_v[fs], dnT_m[fs], w.d, gate=Hu[:, fs])
     dWu_r, _ = O.masked_dw(dHc_b, X, up_m[fs])
-    keep = ~gate_flips(o["H"][:, tm(fs)], Hc_b, Hc_r).any(axis=0)
-    assert keep.sum() >= len(fs) - 2
     udH2 = ulp_bf16(dHc_b) ** 2
-    X2 = O.bf16_to_f32(X) ** 2
-    assert_close(o["dW_up"][tm(fs[keep])], dWu_r[keep], "dW_up rows", propagated(udH2[:, keep].T, X2))
-    assert_close(o["db_up"][tm(fs[keep])], O.colsum(dHc_b)[keep], "db_up entries",
-                 4 * np.sqrt(udH2[:, keep].sum(0)))
-    # dW_down[ns, :] = dY[:, ns]^T H on the mask: needs the oracle's whole H
-    _, H_all = O.spmm24_fwd(X, up_v, up_m, w.d, relu=True)
-    dWd_r, _ = O.masked_dw(dY[:, ns], H_all, dn_m[ns])
-    dY2 = O.bf16_to_f32(dY[:, ns]) ** 2
-    assert_close(o["dW_down"][tm(ns)], dWd_r, "dW_down rows", propagated(dY2.T, ulp_bf16(H_all) ** 2))
+    assert_close(o["dW_up"][tm(fs)], dWu_r, "dW_up rows", propagated(udH2.T, O.bf16_to_f32(X) ** 2))
+    assert_close(o["db_up"][tm(fs)], O.colsum(dHc_b), "db_up entries", 4 * np.sqrt(udH2.sum(0)))
+    del dHc_b, udH2, dWu_r
+    # model features: dW_down[ns, :] = dY[:, ns]^T H_used on the mask (undisputed hidden units)
+    dWd_r, _ = O.masked_dw(dY[:, ns], Hu, dn_m[ns])
+    bound = propagated(O.bf16_to_f32(dY[:, ns]).T ** 2, ulp_bf16(Hu) ** 2)
+    assert_close(o["dW_down"][tm(ns)][:, tm(kf_all)], dWd_r[:, kf_all], "dW_down rows", bound[:, kf_all])
     assert_close(o["db_down"][tm(ns)], O.colsum(dY[:, ns]), "db_down entries")
