@@ -33,6 +33,32 @@ import torch  # noqa: E402
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SPARSE_RATIO = 2.0  # nominal 2:4-sparse / dense tensor throughput
+# DRAM bytes per launch of the dominant kernel, from an ncu capture; used only while
+# the kernel's sources are the ones that were captured.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spmm_kernel_dram_traffic.json")
+KERNEL_SOURCES = ("gemm24_kernels.cu", "p24_ptx.cuh", "p24_internal.h")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "semi_structured_sparse_prune24_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic(workload: str) -> float | None:
+    """Per-launch DRAM bytes (read + write) of spmm_kernel at this workload, or None
+    when no capture matches the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("per_launch_bytes", {}).get(workload)
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -254,7 +280,8 @@ def run_ours(args, world, rank, local):
     dominant = max(breakdown, key=lambda n: breakdown[n]["ms_per_step"])
     dk = kernels[dominant]
     roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": breakdown[dominant]["achieved"],
-                "peak": dk["peak"], "unit": dk["unit"], "frac": breakdown[dominant]["frac"], "traffic": None,
+                "peak": dk["peak"], "unit": dk["unit"], "frac": breakdown[dominant]["frac"],
+                "traffic": captured_traffic(args.workload) if dominant.startswith("spmm_kernel") else None,
                 "peak_source": f"{peak_src} bf16_tflops_sustained" +
                                (" x 2 (nominal 2:4 ratio)" if dk["peak"] == sparse_peak else "")
                                if dk["unit"] == "TFLOP/s" else f"{peak_src} hbm_gbs"}
