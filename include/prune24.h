@@ -229,6 +229,7 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
 
 /* Flags of ffn24_step. */
 #define P24_STEP_ACT24 0x1u /* 2:4-prune ReLU(up) and feed it as the sparse operand of down */
+#define P24_STEP_KEEP_MASKS 0x2u /* use the caller's compressed weights as they are (fixed masks) */
 
 /*
  * One FFN layer (up -> ReLU -> down), forward and backward, every matmul 2:4
@@ -247,6 +248,17 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
  *   activation); b_up, db_up : fp32 [ffn];  b_down, db_down : fp32 [d].
  *   b_up / b_down may be NULL (no bias); db_up / db_down may be NULL.
  * d % 8 == 0 and ffn % 8 == 0.
+ * Compressed weights (caller buffers, optional unless P24_STEP_KEEP_MASKS):
+ *   up_fwd [ffn, d] and down_fwd [d, ffn]: the forward 2:4 weights;
+ *   up_bwdT [d, ffn] and down_bwdT [ffn, d]: their double-pruned transposes;
+ *   W_down_masked : bf16 [d, ffn] (row stride ffn), W_down on its 2:4 mask, the
+ *   dense operand of the down GEMM under P24_STEP_ACT24.
+ *   Without P24_STEP_KEEP_MASKS (gradual magnitude pruning, ESPLAG "Research
+ *   Topic"): the step prunes W_up and W_down afresh and writes the results to
+ *   these buffers where given (NULL: kept in the workspace).
+ *   With P24_STEP_KEEP_MASKS (fixed masks): the step reads them as they are,
+ *   prunes nothing and does not read W_up / W_down (which may be NULL); the four
+ *   compressed buffers (and W_down_masked under P24_STEP_ACT24) are required.
  */
 typedef struct {
   int64_t M, d, ffn;
@@ -264,6 +276,11 @@ typedef struct {
   void* dW_down;
   float* db_up;
   float* db_down;
+  p24_sparse* up_fwd;
+  p24_sparse* up_bwdT;
+  p24_sparse* down_fwd;
+  p24_sparse* down_bwdT;
+  void* W_down_masked;
 } p24_ffn_args;
 
 /* Device workspace ffn24_step needs for these sizes (compressed weights, dH, ...). */
@@ -275,7 +292,8 @@ int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* st
  * (cudaEvent_t handles) on `stream` around each phase of the step, for
  * per-kernel timing without a synchronisation: events[2p] before and
  * events[2p+1] after phase p, for p < min(P24_STEP_PHASES, n_events / 2).
- * Phases: 0 prune+double-prune W_up, 1 the same for W_down, 2 up forward (H),
+ * Phases: 0 prune+double-prune W_up, 1 the same for W_down (both empty with
+ * P24_STEP_KEEP_MASKS), 2 up forward (H),
  * 3 down forward (Y), 4 down backward dX (dH and db_up), 5 db_down, 6 dW_down,
  * 7 up backward dX, 8 dW_up. events may be NULL (then identical to ffn24_step).
  */

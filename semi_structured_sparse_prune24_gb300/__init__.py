@@ -5,12 +5,18 @@ sm_103a under csrc/). This package is its thin Python binding: the functions
 below carry the C names and only marshal torch tensors into pointers, sizes
 and strides. There is no CPU fallback.
 """
-from ._native import (P24_EPI_ACT24, P24_EPI_BIAS, P24_EPI_RELU, P24_STEP_ACT24, P24Error, Sparse24,
-                      STEP_PHASE_NAMES, STEP_PHASES, ffn24_step, ffn24_workspace_size, p24_launch_count, ld_meta, ld_vals, lib, masked_dw_gemm, p24_colsum,
-                      p24_query_status, p24_selftest_timeout, prune24_compress, prune24_compress_both, prune24_transpose_repack,
+from ._native import (P24_EPI_ACT24, P24_EPI_BIAS, P24_EPI_RELU, P24_STEP_ACT24, P24_STEP_KEEP_MASKS, STEP_PHASE_NAMES,
+                      STEP_PHASES, STEP_WEIGHTS, P24Error, Sparse24, ffn24_step, ffn24_workspace_size, ld_meta, ld_vals,
+                      lib, masked_dw_gemm, p24_colsum, p24_colsum_noalloc, p24_launch_count, p24_query_status,
+                      p24_selftest_timeout, prune24_compress, prune24_compress_both, prune24_transpose_repack,
                       spmm24_bwd_dx, spmm24_fwd, spmm24_fwd_sparse_act)
 
-__all__ = ["STEP_PHASES", "STEP_PHASE_NAMES", "p24_launch_count", "P24Error", "Sparse24", "ffn24_step", "ffn24_workspace_size", "ld_meta", "ld_vals", "lib",
-           "masked_dw_gemm", "p24_colsum", "p24_query_status", "p24_selftest_timeout", "prune24_compress", "prune24_compress_both",
-           "prune24_transpose_repack", "spmm24_bwd_dx", "spmm24_fwd", "spmm24_fwd_sparse_act",
-           "P24_EPI_ACT24", "P24_EPI_BIAS", "P24_EPI_RELU", "P24_STEP_ACT24"]
+__all__ = [
+    "P24Error", "Sparse24", "lib", "ld_meta", "ld_vals",
+    "prune24_compress", "prune24_compress_both", "prune24_transpose_repack",
+    "spmm24_fwd", "spmm24_fwd_sparse_act", "spmm24_bwd_dx", "masked_dw_gemm",
+    "p24_colsum", "p24_colsum_noalloc", "ffn24_step", "ffn24_workspace_size",
+    "p24_launch_count", "p24_query_status", "p24_selftest_timeout",
+    "STEP_PHASES", "STEP_PHASE_NAMES", "STEP_WEIGHTS",
+    "P24_EPI_ACT24", "P24_EPI_BIAS", "P24_EPI_RELU", "P24_STEP_ACT24", "P24_STEP_KEEP_MASKS",
+]

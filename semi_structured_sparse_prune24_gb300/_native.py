@@ -19,6 +19,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 P24_OK, P24_EINVAL, P24_EALIGN, P24_ECUDA, P24_ETIMEOUT, P24_EUNSUPPORTED, P24_ENOSPACE = 0, -1, -2, -3, -4, -5, -6
 P24_EPI_BIAS, P24_EPI_RELU, P24_EPI_ACT24 = 0x1, 0x2, 0x4
 P24_STEP_ACT24 = 0x1
+P24_STEP_KEEP_MASKS = 0x2
 
 
 class P24Error(RuntimeError):
@@ -37,7 +38,9 @@ class p24_ffn_args(C.Structure):
                 ("X", C.c_void_p), ("W_up", C.c_void_p), ("b_up", C.c_void_p), ("W_down", C.c_void_p),
                 ("b_down", C.c_void_p), ("dY", C.c_void_p), ("Y", C.c_void_p), ("H", C.c_void_p),
                 ("dX", C.c_void_p), ("dW_up", C.c_void_p), ("dW_down", C.c_void_p), ("db_up", C.c_void_p),
-                ("db_down", C.c_void_p)]
+                ("db_down", C.c_void_p), ("up_fwd", C.POINTER(p24_sparse)), ("up_bwdT", C.POINTER(p24_sparse)),
+                ("down_fwd", C.POINTER(p24_sparse)), ("down_bwdT", C.POINTER(p24_sparse)),
+                ("W_down_masked", C.c_void_p)]
 
 
 def _load() -> C.CDLL:
@@ -278,16 +281,35 @@ STEP_PHASE_NAMES = ("prune_up", "prune_down", "up_fwd", "down_fwd", "down_bwd_dx
                     "up_bwd_dx", "dW_up")
 
 
+STEP_WEIGHTS = ("up_fwd", "up_bwdT", "down_fwd", "down_bwdT")
+
+
 def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict | None = None,
-               workspace: torch.Tensor | None = None, stream=None, events=None) -> dict:
+               workspace: torch.Tensor | None = None, stream=None, events=None, weights: dict | None = None,
+               keep_masks: bool = False) -> dict:
     """One 2:4 FFN layer fwd+bwd; returns dict(Y, H, dX, dW_up, dW_down, db_up, db_down).
 
     events: optional ctypes array of 2 * STEP_PHASES raw cudaEvent_t handles, recorded
-    before/after each phase (see ffn24_step_traced in include/prune24.h)."""
+    before/after each phase (see ffn24_step_traced in include/prune24.h).
+    weights: optional caller-owned compressed weights, a dict with Sparse24 entries
+    up_fwd [ffn, d], up_bwdT [d, ffn], down_fwd [d, ffn], down_bwdT [ffn, d] and a bf16
+    W_down_masked [d, ffn]. Without keep_masks the step prunes W_up / W_down afresh and
+    writes the results there; with keep_masks=True it uses them as they are (fixed
+    masks) and W_up / W_down are not read (they may be None)."""
     M, d, _ = _mat(X, name="X")
-    ffn = W_up.shape[0]
+    w = dict(weights or {})
+    if keep_masks:
+        missing = [k for k in STEP_WEIGHTS + (("W_down_masked",) if act24 else ()) if w.get(k) is None]
+        if missing:
+            raise ValueError(f"keep_masks needs the compressed weights: missing {missing}")
+        ffn = w["up_fwd"].rows
+    else:
+        ffn = W_up.shape[0]
     dev = X.device
-    for t, name, shape in ((W_up, "W_up", (ffn, d)), (W_down, "W_down", (d, ffn)), (dY, "dY", (M, d))):
+    for t, name, shape in ((W_up, "W_up", (ffn, d)), (W_down, "W_down", (d, ffn)), (dY, "dY", (M, d)),
+                           (w.get("W_down_masked"), "W_down_masked", (d, ffn))):
+        if t is None:
+            continue
         _mat(t, name=name)
         if tuple(t.shape) != shape or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous {shape} tensor")
@@ -303,10 +325,15 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     need = ffn24_workspace_size(M, d, ffn, act24)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    a = p24_ffn_args(M, d, ffn, P24_STEP_ACT24 if act24 else 0, X.data_ptr(), W_up.data_ptr(), _ptr(b_up),
-                     W_down.data_ptr(), _ptr(b_down), dY.data_ptr(), o["Y"].data_ptr(), o["H"].data_ptr(),
+    flags = (P24_STEP_ACT24 if act24 else 0) | (P24_STEP_KEEP_MASKS if keep_masks else 0)
+    a = p24_ffn_args(M, d, ffn, flags, X.data_ptr(), _ptr(W_up), _ptr(b_up),
+                     _ptr(W_down), _ptr(b_down), dY.data_ptr(), o["Y"].data_ptr(), o["H"].data_ptr(),
                      o["dX"].data_ptr(), o["dW_up"].data_ptr(), o["dW_down"].data_ptr(), _ptr(o["db_up"]),
                      _ptr(o["db_down"]))
+    structs = {k: w[k].c() for k in STEP_WEIGHTS if w.get(k) is not None}  # alive for the call
+    for k, st in structs.items():
+        setattr(a, k, C.pointer(st))
+    a.W_down_masked = _ptr(w.get("W_down_masked"))
     if events is None:
         _check(lib.ffn24_step(C.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "ffn24_step")
     else:

@@ -266,12 +266,28 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
                       int n_events) {
   if (!a) return P24_EINVAL;
   if (n_events < 0 || (n_events > 0 && !events)) return P24_EINVAL;
-  if (a->flags & ~P24_STEP_ACT24) return P24_EINVAL;
+  if (a->flags & ~(P24_STEP_ACT24 | P24_STEP_KEEP_MASKS)) return P24_EINVAL;
   const int64_t M = a->M, d = a->d, ffn = a->ffn;
   if (M < 0 || d <= 0 || ffn <= 0 || d % 8 != 0 || ffn % 8 != 0) return P24_EINVAL;
   const bool act24 = (a->flags & P24_STEP_ACT24) != 0;
-  P24_TRY(check_dense(a->W_up, ffn, d, d));
-  P24_TRY(check_dense(a->W_down, d, ffn, ffn));
+  const bool keep = (a->flags & P24_STEP_KEEP_MASKS) != 0;
+  // caller's compressed weights: required with fixed masks, optional otherwise
+  const p24_sparse* cw[4] = {a->up_fwd, a->up_bwdT, a->down_fwd, a->down_bwdT};
+  const int64_t cw_rows[4] = {ffn, d, d, ffn}, cw_cols[4] = {d, ffn, ffn, d};
+  for (int i = 0; i < 4; ++i) {
+    if (!cw[i]) {
+      if (keep) return P24_EINVAL;
+      continue;
+    }
+    P24_TRY(check_sparse(cw[i]));
+    if (cw[i]->rows != cw_rows[i] || cw[i]->cols != cw_cols[i]) return P24_EINVAL;
+  }
+  if (keep && act24 && !a->W_down_masked) return P24_EINVAL;
+  if (a->W_down_masked) P24_TRY(check_dense(a->W_down_masked, d, ffn, ffn));
+  if (!keep) {
+    P24_TRY(check_dense(a->W_up, ffn, d, d));
+    P24_TRY(check_dense(a->W_down, d, ffn, ffn));
+  }
   P24_TRY(check_dense(a->dW_up, ffn, d, d));
   P24_TRY(check_dense(a->dW_down, d, ffn, ffn));
   if (M > 0) {
@@ -306,9 +322,22 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
     P24_TRY(mark(ph, 1));     \
   } while (0)
 
-  // 1. fresh 2:4 masks of both weights, and their double-pruned transposes
-  P24_PHASE(0, P24_TRY(cuda_status(launch_compress_both(a->W_up, ffn, d, d, L.up_fwd, L.up_bwdT, nullptr, 0, s))));
-  P24_PHASE(1, P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT, wdm, ffn, s))));
+  // caller buffers replace the workspace's copies
+  if (a->up_fwd) L.up_fwd = *a->up_fwd;
+  if (a->up_bwdT) L.up_bwdT = *a->up_bwdT;
+  if (a->down_fwd) L.dn_fwd = *a->down_fwd;
+  if (a->down_bwdT) L.dn_bwdT = *a->down_bwdT;
+  if (a->W_down_masked) wdm = a->W_down_masked;
+  // 1. fresh 2:4 masks of both weights, and their double-pruned transposes (GMP);
+  //    with fixed masks the caller's compressed weights are used as they are
+  P24_PHASE(0, {
+    if (!keep) P24_TRY(cuda_status(launch_compress_both(a->W_up, ffn, d, d, L.up_fwd, L.up_bwdT, nullptr, 0, s)));
+  });
+  P24_PHASE(1, {
+    if (!keep)
+      P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT,
+                                               (act24 || a->W_down_masked) ? wdm : nullptr, ffn, s)));
+  });
   if (M == 0) {
     if (a->db_up) P24_TRY(cuda_status(cudaMemsetAsync(a->db_up, 0, ffn * 4, s)));
     if (a->db_down) P24_TRY(cuda_status(cudaMemsetAsync(a->db_down, 0, d * 4, s)));

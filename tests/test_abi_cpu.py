@@ -95,6 +95,18 @@ def test_host_validation_rejects_before_launch(native):
     assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
     a.d, a.flags = 16, 0x8
     assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
+    # fixed masks need the caller's compressed weights (and W_down on its mask with ACT24)
+    a.flags = native.P24_STEP_KEEP_MASKS
+    assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
+    up, upT = _sp(fake, fake, 16, 16, 8, 16, native), _sp(fake, fake, 16, 16, 8, 16, native)
+    dn, dnT = _sp(fake, fake, 16, 16, 8, 16, native), _sp(fake, fake, 16, 16, 8, 16, native)
+    a.up_fwd, a.up_bwdT, a.down_fwd, a.down_bwdT = (C.pointer(x) for x in (up, upT, dn, dnT))
+    a.flags = native.P24_STEP_KEEP_MASKS | native.P24_STEP_ACT24
+    assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
+    # a compressed weight of the wrong shape
+    a.flags = native.P24_STEP_KEEP_MASKS
+    a.up_fwd = C.pointer(_sp(fake, fake, 16, 8, 8, 16, native))
+    assert L.ffn24_step(C.byref(a), fake, 1 << 30, None) == EINVAL
 
 
 def test_workspace_sizes_grow_with_the_problem(native):

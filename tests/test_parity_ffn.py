@@ -238,3 +238,66 @@ def test_ffn_step_large_workloads_sampled(P, name):
     bound = propagated(O.bf16_to_f32(dY[:, ns]).T ** 2, ulp_bf16(Hu) ** 2)
     assert_close(o["dW_down"][tm(ns)][:, tm(kf_all)], dWd_r[:, kf_all], "dW_down rows", bound[:, kf_all])
     assert_close(o["db_down"][tm(ns)], O.colsum(dY[:, ns]), "db_down entries")
+
+
+def oracle_weights(P, W_up_bits, W_down_bits, ffn, d, device="cuda"):
+    """Compressed weights and W_down on its mask, computed by the oracle and uploaded
+    into the binding's buffers."""
+    from tests.conftest import from_bits
+    bufs = {"up_fwd": P.Sparse24.empty(ffn, d, device), "up_bwdT": P.Sparse24.empty(d, ffn, device),
+            "down_fwd": P.Sparse24.empty(d, ffn, device), "down_bwdT": P.Sparse24.empty(ffn, d, device)}
+    uv, um = O.compress24(W_up_bits, bufs["up_fwd"].ldv, bufs["up_fwd"].ldm)
+    dv, dm = O.compress24(W_down_bits, bufs["down_fwd"].ldv, bufs["down_fwd"].ldm)
+    ref = {"up_fwd": (uv, um), "down_fwd": (dv, dm),
+           "up_bwdT": O.double_prune(uv, um, ffn, d, bufs["up_bwdT"].ldv, bufs["up_bwdT"].ldm),
+           "down_bwdT": O.double_prune(dv, dm, d, ffn, bufs["down_bwdT"].ldv, bufs["down_bwdT"].ldm)}
+    for k, (v, m) in ref.items():
+        bufs[k].vals.copy_(from_bits(v, device))
+        bufs[k].meta.copy_(torch.from_numpy(m).to(device))
+    bufs["W_down_masked"] = from_bits(O.decompress24(dv, dm, ffn), device)
+    return bufs, ref
+
+
+@pytest.mark.parametrize("act24", [False, True])
+def test_ffn_step_writes_fresh_masks_to_caller_buffers(P, act24):
+    """Gradual magnitude pruning with caller-owned compressed weights: the step's
+    fresh masks land in the caller's buffers bit for bit, and a fixed-mask step
+    reading those buffers (W_up / W_down not passed) reproduces the outputs."""
+    w = FFNWorkload("small", 200, 264, 392, 0.05)
+    inp = ffn_inputs(w, seed=12, device="cuda", bias=True)
+    bufs = {"up_fwd": P.Sparse24.empty(w.ffn, w.d), "up_bwdT": P.Sparse24.empty(w.d, w.ffn),
+            "down_fwd": P.Sparse24.empty(w.d, w.ffn), "down_bwdT": P.Sparse24.empty(w.ffn, w.d),
+            "W_down_masked": torch.empty((w.d, w.ffn), dtype=torch.bfloat16, device="cuda")}
+    o1 = P.ffn24_step(inp["X"], inp["W_up"], inp["b_up"], inp["W_down"], inp["b_down"], inp["dY"], act24=act24,
+                      weights=bufs)
+    torch.cuda.synchronize()
+    _, ref = oracle_weights(P, bits_of(inp["W_up"]), bits_of(inp["W_down"]), w.ffn, w.d, device="cpu")
+    for k, (rv, rm) in ref.items():
+        gv, gm = sparse_bits(bufs[k])
+        assert_bits_equal(gv, rv, k + " vals")
+        assert_bits_equal(gm, rm, k + " meta")
+    assert_bits_equal(bits_of(bufs["W_down_masked"]), O.decompress24(*ref["down_fwd"], w.ffn), "W_down_masked")
+    o2 = P.ffn24_step(inp["X"], None, inp["b_up"], None, inp["b_down"], inp["dY"], act24=act24,
+                      weights=bufs, keep_masks=True)
+    torch.cuda.synchronize()
+    assert P.p24_query_status() == 0
+    for k in ("H", "Y", "dX", "dW_up", "dW_down"):
+        assert_bits_equal(bits_of(o2[k]), bits_of(o1[k]), k + " (fixed masks vs fresh)")
+    assert torch.equal(o2["db_down"], o1["db_down"])
+    torch.testing.assert_close(o2["db_up"], o1["db_up"], rtol=1e-5, atol=1e-4)   # fp32 atomics: order may differ
+
+
+@pytest.mark.parametrize("act24", [False, True])
+def test_ffn_step_fixed_masks_against_the_oracle(P, act24):
+    """Fixed masks taken from another weight W0 (compressed by the oracle and uploaded):
+    the step must compute exactly the oracle's step on W0, whatever W_up / W_down hold."""
+    w = FFNWorkload("small", 200, 264, 392, 0.05)
+    inp = ffn_inputs(w, seed=13, device="cuda", bias=True)
+    inp0 = ffn_inputs(w, seed=14, device="cuda", bias=True)          # W0 = inp0's weights
+    bufs, _ = oracle_weights(P, bits_of(inp0["W_up"]), bits_of(inp0["W_down"]), w.ffn, w.d)
+    o = P.ffn24_step(inp["X"], None, inp["b_up"], None, inp["b_down"], inp["dY"], act24=act24, weights=bufs,
+                     keep_masks=True)
+    torch.cuda.synchronize()
+    assert P.p24_query_status() == 0
+    ref_inp = dict(inp, W_up=inp0["W_up"], W_down=inp0["W_down"])
+    compare_step(o, oracle_step(ref_inp, act24), w, act24)
