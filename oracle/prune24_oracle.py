@@ -31,7 +31,10 @@ used here (each one is listed with its reason in the design notes):
     rounded to bf16 with round-half-to-even;
   * ReLU'(0) = 0;
   * the weight gradient is masked by the positions the forward metadata
-    selects, and bias gradients are fp32 column sums of the bf16 gradients.
+    selects, and bias gradients are fp32 column sums of the bf16 gradients;
+  * SLOPE's low-rank adapters are read as a dense rank-r term beside each sparse
+    weight, X W_s^T + (X R^T) L^T, trained with its exact gradients; the
+    intermediate products X R^T and dY L are stored in bf16.
 
 All bf16 tensors are numpy uint16 arrays of bit patterns.
 """
@@ -191,14 +194,19 @@ def relu_f32(x: np.ndarray) -> np.ndarray:
 
 
 def spmm24_fwd(X: np.ndarray, vals: np.ndarray, meta: np.ndarray, K: int,
-               bias: np.ndarray | None = None, relu: bool = False):
+               bias: np.ndarray | None = None, relu: bool = False, adapter=None):
     """Y = act(X . W^T + bias) with W given compressed 2:4 along K.
 
     X [M, K] bf16 bits; vals/meta the compressed W [N, K]; bias fp32 [N].
+    adapter (optional): (T, L), bf16 bits T = X R^T [M, r] and L [N, r]; the
+    low-rank term T . L^T joins the sum before bias and activation [SLOPE].
     Returns (Y_ref fp32 before rounding, Y bf16 bits).
     """
     W = decompress24(vals, meta, K)
     Y = matmul_nt_f32(bf16_to_f32(X), bf16_to_f32(W))
+    if adapter is not None:
+        T, L = adapter
+        Y = (Y + matmul_nt_f32(bf16_to_f32(T), bf16_to_f32(L))).astype(np.float32)
     if bias is not None:
         Y = (Y + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
     if relu:
@@ -207,14 +215,20 @@ def spmm24_fwd(X: np.ndarray, vals: np.ndarray, meta: np.ndarray, K: int,
 
 
 def spmm24_bwd_dx(dY: np.ndarray, vals_t: np.ndarray, meta_t: np.ndarray, N: int,
-                  gate: np.ndarray | None = None):
+                  gate: np.ndarray | None = None, adapter=None):
     """dX = dY . W_bwd, with W_bwd^T [K, N] given compressed 2:4 along N  [SLOPE].
 
     gate (optional, bf16 bits [M, K]): the forward ReLU output; dX is zeroed
-    where gate <= 0 (ReLU'(0) = 0). Returns (dX_ref fp32, dX bf16 bits).
+    where gate <= 0 (ReLU'(0) = 0).
+    adapter (optional): (U, R), bf16 bits U = dY L [M, r] and R [r, K]; the
+    adapter's input gradient U . R joins the sum before the gate [SLOPE].
+    Returns (dX_ref fp32, dX bf16 bits).
     """
     WbT = decompress24(vals_t, meta_t, N)            # [K, N]
     dX = matmul_nt_f32(bf16_to_f32(dY), bf16_to_f32(WbT))
+    if adapter is not None:
+        U, R = adapter
+        dX = (dX + np.matmul(bf16_to_f32(U), bf16_to_f32(R))).astype(np.float32)
     if gate is not None:
         dX = np.where(bf16_to_f32(gate) > 0, dX, np.float32(0)).astype(np.float32)
     return dX, f32_to_bf16(dX)
@@ -241,8 +255,24 @@ def colsum(G: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # The FFN training step  [ESPLAG "Research Topic"; SLOPE; TO24 abstract]
 # ----------------------------------------------------------------------------
+def dense_nt(A: np.ndarray, B: np.ndarray):
+    """C = A . B^T for bf16 bits A [M, K], B [N, K]; fp32 accumulation.
+    Returns (C_ref fp32, C bf16 bits). The low-rank products of SLOPE's
+    adapters (T = X R^T, U = dY L with L stored as L^T) are of this form."""
+    C = matmul_nt_f32(bf16_to_f32(A), bf16_to_f32(B))
+    return C, f32_to_bf16(C)
+
+
+def dense_tn(A: np.ndarray, B: np.ndarray):
+    """C = A^T . B for bf16 bits A [M, N], B [M, K] (a contraction over the tokens
+    M, like the weight gradient but unmasked): the adapter gradients dL and dR.
+    Returns (C_ref fp32, C bf16 bits)."""
+    C = np.matmul(bf16_to_f32(A).T, bf16_to_f32(B)).astype(np.float32)
+    return C, f32_to_bf16(C)
+
+
 def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
-             H_override: np.ndarray | None = None) -> dict:
+             H_override: np.ndarray | None = None, adapters: dict | None = None) -> dict:
     """One up -> ReLU -> down FFN layer, forward and backward, all matmuls 2:4.
 
     X [M, d], W_up [ffn, d], W_down [d, ffn], dY [M, d]: bf16 bits; biases fp32.
@@ -255,6 +285,15 @@ def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
       dH = (dY W_down_bwd) * [H_used > 0];  db_up = colsum(dH);  db_down = colsum(dY);
       dW_down = (dY^T H_used) on mask_down;  dX = dH W_up_bwd;  dW_up = (dH^T X) on mask_up.
     H_override replaces the computed bf16 H (to chain another implementation's H).
+    adapters (optional) adds SLOPE's low-rank adapters [SLOPE abstract: "low-rank
+    adapters" beside the double-pruned sparse weights], each linear becoming
+    X W_s^T + (X R^T) L^T: a dict of bf16 bits L_up [ffn, r], R_up [r, d],
+    L_down [d, r], R_down [r, ffn]. Then also
+      T_up = X R_up^T,  T_down = H_used R_down^T          (bf16, [M, r]);
+      U_down = dY L_down,  U_up = dH L_up                  (bf16, [M, r]);
+      dH and dX gain U_down R_down and U_up R_up (before the gate for dH);
+      dL_down = dY^T T_down,  dR_down = U_down^T H_used,
+      dL_up = dH^T T_up,      dR_up = U_up^T X             (bf16).
     """
     ffn, d = W_up.shape
     out: dict = {}
@@ -265,7 +304,12 @@ def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
     out.update(up_vals=up_v, up_meta=up_m, down_vals=dn_v, down_meta=dn_m,
                upT_vals=upT_v, upT_meta=upT_m, downT_vals=dnT_v, downT_meta=dnT_m)
 
-    H_ref, H = spmm24_fwd(X, up_v, up_m, d, bias=b_up, relu=True)
+    ad = adapters
+    if ad is not None:
+        _, T_up = dense_nt(X, ad["R_up"])
+        out["T_up"] = T_up
+    H_ref, H = spmm24_fwd(X, up_v, up_m, d, bias=b_up, relu=True,
+                          adapter=None if ad is None else (T_up, ad["L_up"]))
     if H_override is not None:
         H = np.asarray(H_override, dtype=np.uint16)
     out.update(H_ref=H_ref, H=H)
@@ -279,19 +323,34 @@ def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
 
     # Y = H_used . W_down_pruned^T + b_down. With act24 the sparse operand is
     # Hs and the dense one W_down on its mask; the product is the same.
-    Y_ref, Y = spmm24_fwd(H_used, dn_v, dn_m, ffn, bias=b_down, relu=False)
+    if ad is not None:
+        _, T_dn = dense_nt(H_used, ad["R_down"])
+        _, U_dn = dense_nt(dY, ad["L_down"].T)
+        out.update(T_down=T_dn, U_down=U_dn)
+    Y_ref, Y = spmm24_fwd(H_used, dn_v, dn_m, ffn, bias=b_down, relu=False,
+                          adapter=None if ad is None else (T_dn, ad["L_down"]))
     out.update(Y_ref=Y_ref, Y=Y)
 
-    dH_ref, dH = spmm24_bwd_dx(dY, dnT_v, dnT_m, d, gate=H_used)
+    dH_ref, dH = spmm24_bwd_dx(dY, dnT_v, dnT_m, d, gate=H_used,
+                               adapter=None if ad is None else (U_dn, ad["R_down"]))
     out.update(dH_ref=dH_ref, dH=dH)
     out["db_up"] = colsum(dH)
     out["db_down"] = colsum(dY)
     dWd_ref, dWd = masked_dw(dY, H_used, dn_m)
     out.update(dW_down_ref=dWd_ref, dW_down=dWd)
-    dX_ref, dX = spmm24_bwd_dx(dH, upT_v, upT_m, ffn, gate=None)
+    if ad is not None:
+        _, U_up = dense_nt(dH, ad["L_up"].T)
+        out["U_up"] = U_up
+    dX_ref, dX = spmm24_bwd_dx(dH, upT_v, upT_m, ffn, gate=None,
+                               adapter=None if ad is None else (U_up, ad["R_up"]))
     out.update(dX_ref=dX_ref, dX=dX)
     dWu_ref, dWu = masked_dw(dH, X, up_m)
     out.update(dW_up_ref=dWu_ref, dW_up=dWu)
+    if ad is not None:
+        for name, (a, b) in (("dL_down", (dY, T_dn)), ("dR_down", (U_dn, H_used)),
+                             ("dL_up", (dH, T_up)), ("dR_up", (U_up, X))):
+            ref, bits = dense_tn(a, b)
+            out[name + "_ref"], out[name] = ref, bits
     return out
 
 

@@ -329,3 +329,94 @@ def test_planted_nibble_order_mistake_is_caught(ex, monkeypatch):
     monkeypatch.setattr(O, "compress24", swapped)
     with pytest.raises(AssertionError):
         test_worked_example_compress_and_double_prune(ex)
+
+
+# ---------------------------------------------------------------- SLOPE adapters
+def _adapter_case(seed=21, M=24, d=32, ffn=64, r=16, act24=False):
+    """Integer-valued inputs (|x| <= 1 or 2): every sum below is an integer far below
+    2**24 and every bf16 intermediate (T, U, H, dH) is an integer below 2**8, so the
+    oracle's fp32 results are exact and can be compared with fp64 compositions."""
+    ints = lambda shape, s, lo=-1, hi=2: bf(np.random.default_rng(s).integers(lo, hi, size=shape).astype(np.float32))  # noqa: E731
+    X, dY = ints((M, d), seed), ints((M, d), seed + 1)
+    W_up, W_dn = ints((ffn, d), seed + 2, -2, 3), ints((d, ffn), seed + 3, -2, 3)
+    ad = {"L_up": ints((ffn, r), seed + 4), "R_up": ints((r, d), seed + 5),
+          "L_down": ints((d, r), seed + 6), "R_down": ints((r, ffn), seed + 7)}
+    b_up = np.zeros(ffn, np.float32)
+    b_dn = np.zeros(d, np.float32)
+    out = O.ffn_step(X, W_up, b_up, W_dn, b_dn, dY, act24=act24, adapters=ad)
+    f = lambda a: O.bf16_to_f32(a).astype(np.float64)  # noqa: E731
+    return out, ad, f, X, dY, ffn, d
+
+
+@pytest.mark.parametrize("act24", [False, True])
+def test_adapter_forward_is_sparse_plus_low_rank(act24):
+    """[SLOPE] each linear is the pruned weight plus the rank-r product L R:
+    X W_s^T + (X R^T) L^T == X (W_s + L R)^T, exactly."""
+    o, ad, f, X, dY, ffn, d = _adapter_case(act24=act24)
+    assert np.abs(f(o["T_up"])).max() < 256 and np.abs(f(o["H"])).max() < 256   # exact in bf16
+    Wu = f(O.decompress24(o["up_vals"], o["up_meta"], d)) + f(ad["L_up"]) @ f(ad["R_up"])
+    assert np.array_equal(o["H_ref"].astype(np.float64), np.maximum(f(X) @ Wu.T, 0))
+    Wd = f(O.decompress24(o["down_vals"], o["down_meta"], ffn)) + f(ad["L_down"]) @ f(ad["R_down"])
+    assert np.array_equal(o["Y_ref"].astype(np.float64), f(o["H_used"]) @ Wd.T)
+
+
+def test_adapter_input_gradients_compose():
+    """dH = (dY (W_down_bwd + L_down R_down)) * [H > 0] and dX = dH (W_up_bwd + L_up R_up):
+    the double-pruned sparse weight plus the exact adapter, exactly."""
+    o, ad, f, X, dY, ffn, d = _adapter_case()
+    Wdb = f(O.decompress24(o["downT_vals"], o["downT_meta"], d)).T + f(ad["L_down"]) @ f(ad["R_down"])
+    dH = (f(dY) @ Wdb) * (f(o["H_used"]) > 0)
+    assert np.array_equal(o["dH_ref"].astype(np.float64), dH)
+    Wub = f(O.decompress24(o["upT_vals"], o["upT_meta"], ffn)).T + f(ad["L_up"]) @ f(ad["R_up"])
+    assert np.array_equal(o["dX_ref"].astype(np.float64), f(o["dH"]) @ Wub)
+
+
+def _adjoint_residuals(o, ad, f, X, dY):
+    """Each adapter gradient G of a parameter P must satisfy the defining identity of a
+    gradient of the bilinear loss sum(G_out * out): sum(G_out * out[P'']) == sum(G * P'')
+    for any direction P'' (here a random integer one), with out[P''] the output the
+    linear produces when P is replaced by P''."""
+    rng = np.random.default_rng(99)
+    res = {}
+    H, dH = f(o["H_used"]), f(o["dH"])
+    # down linear: Y += T_down L_down^T, T_down = H R_down^T; upstream gradient dY
+    Lp = rng.integers(-2, 3, size=ad["L_down"].shape).astype(np.float64)
+    res["dL_down"] = np.sum(f(dY) * (f(o["T_down"]) @ Lp.T)) - np.sum(o["dL_down_ref"].astype(np.float64) * Lp)
+    Rp = rng.integers(-2, 3, size=ad["R_down"].shape).astype(np.float64)
+    res["dR_down"] = np.sum(f(dY) * ((H @ Rp.T) @ f(ad["L_down"]).T)) - np.sum(o["dR_down_ref"].astype(np.float64) * Rp)
+    # up linear: pre-activation += T_up L_up^T, T_up = X R_up^T; upstream gradient dH
+    Lp = rng.integers(-2, 3, size=ad["L_up"].shape).astype(np.float64)
+    res["dL_up"] = np.sum(dH * (f(o["T_up"]) @ Lp.T)) - np.sum(o["dL_up_ref"].astype(np.float64) * Lp)
+    Rp = rng.integers(-2, 3, size=ad["R_up"].shape).astype(np.float64)
+    res["dR_up"] = np.sum(dH * ((f(X) @ Rp.T) @ f(ad["L_up"]).T)) - np.sum(o["dR_up_ref"].astype(np.float64) * Rp)
+    return res
+
+
+def test_adapter_weight_gradients_satisfy_their_adjoint_identities():
+    """On the exact fp32 gradients (integers below 2**24; their bf16 rounding is pinned
+    with the other roundings); the intermediates they use are exact in bf16."""
+    o, ad, f, X, dY, _, _ = _adapter_case()
+    for name in ("T_up", "T_down", "U_up", "U_down", "H_used", "dH"):
+        assert np.abs(f(o[name])).max() < 256
+    res = _adjoint_residuals(o, ad, f, X, dY)
+    assert all(v == 0 for v in res.values()), res
+    for name in ("dL_down", "dR_down", "dL_up", "dR_up"):
+        assert np.array_equal(o[name], O.f32_to_bf16(o[name + "_ref"]))
+
+
+def test_planted_adapter_gradient_mistake_is_caught(monkeypatch):
+    """dR computed with its operands' roles swapped (X^T U instead of U^T X, shaped
+    back to [r, K]) must fail the adjoint identity."""
+    real = O.dense_tn
+
+    def swapped(A, B):
+        C_ref, C = real(A, B)
+        if A.shape[1] < B.shape[1]:                          # the dR products: [r, K]
+            C_ref2, _ = real(B, A)                           # [K, r]
+            C_ref = C_ref2.T.copy()[::-1].copy()             # a plausible but wrong [r, K]
+            C = O.f32_to_bf16(C_ref)
+        return C_ref, C
+    monkeypatch.setattr(O, "dense_tn", swapped)
+    o, ad, f, X, dY, _, _ = _adapter_case()
+    res = _adjoint_residuals(o, ad, f, X, dY)
+    assert res["dR_down"] != 0 or res["dR_up"] != 0
