@@ -179,6 +179,59 @@ int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* Wbw
                   float* dbias, void* stream);
 
 /*
+ * Low-rank adapters (SLOPE abstract: "low-rank adapters" added beside the
+ * double-pruned sparse weights for the final iterations of pretraining). Read
+ * as a dense rank-r term per linear: Y = X W_s^T + (X R^T) L^T with L [N, r],
+ * R [r, K], trained with its exact gradients. The two products of rank r are
+ * computed once per call with p24_gemm_nt; the sparse GEMMs then add them as
+ * r / 64 extra dense K-steps into the same fp32 accumulator, before the epilogue.
+ * r > 0 and r % 8 == 0 (16-byte rows). Memory is the caller's, as everywhere.
+ *
+ * spmm24_fwd_lowrank -- spmm24_fwd plus the adapter:
+ *   Y = act(X W^T + T L^T + bias),  T : device bf16 [M, ldt] = X R^T (r columns),
+ *   L : device bf16 [N, ldl] (r columns), N = W->rows.  Other arguments as spmm24_fwd.
+ */
+int spmm24_fwd_lowrank(const void* X, int64_t M, int64_t ldx, const p24_sparse* W,
+                       const void* T, int64_t ldt, const void* L, int64_t ldl, int64_t r,
+                       const float* bias, uint32_t flags, void* Y, int64_t ldy,
+                       const p24_sparse* Y24, void* stream);
+
+/*
+ * spmm24_bwd_dx_lowrank -- spmm24_bwd_dx plus the adapter's input gradient:
+ *   dX = (dY W_bwd + U R) * [gate > 0],  U : device bf16 [M, ldu] = dY L
+ *   (r columns), Rt : device bf16 [K, ldrt] = R^T (r columns), K = WbwdT->rows.
+ *   Other arguments (gate, dbias) as spmm24_bwd_dx.
+ */
+int spmm24_bwd_dx_lowrank(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT,
+                          const void* U, int64_t ldu, const void* Rt, int64_t ldrt, int64_t r,
+                          const void* gate, int64_t ldg, void* dX, int64_t lddx,
+                          float* dbias, void* stream);
+
+/*
+ * p24_gemm_nt -- C = A B^T, the adapters' rank-r products (T = X R^T, U = dY L
+ * with L^T as B): A device bf16 [M, lda], B [N, ldb], both K columns; C bf16
+ * [M, ldc]; fp32 accumulation, one rounding. Runs on the sparse GEMM's pipeline
+ * with dense stages only.
+ */
+int p24_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B, int64_t N,
+                int64_t ldb, int64_t K, void* C, int64_t ldc, void* stream);
+
+/*
+ * p24_gemm_tn -- C = A^T B, a contraction over the M tokens, unmasked: the
+ * adapters' weight gradients (dL = dY^T T, dR = U^T X). A device bf16 [M, lda]
+ * (N columns), B [M, ldb] (K columns), C bf16 [N, ldc] (K columns). Runs on the
+ * weight-gradient kernel with the mask off.
+ */
+int p24_gemm_tn(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M,
+                int64_t N, int64_t K, void* C, int64_t ldc, void* stream);
+
+/* p24_transpose -- dst [cols, ldd] = src [rows, lds]^T, bf16 (L^T and R^T for the
+ * adapters' backward products). Any strides (lds >= cols, ldd >= rows); 2-byte
+ * aligned pointers. */
+int p24_transpose(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
+                  int64_t ldd, void* stream);
+
+/*
  * masked_dw_gemm -- weight gradient of a 2:4 linear, kept on the forward mask:
  *   dW = (dY^T . X) * mask(Wfwd), a dense contraction over M in fp32.
  *   dY   : device bf16 [M, lddy], N columns;  X : device bf16 [M, ldx], K columns.

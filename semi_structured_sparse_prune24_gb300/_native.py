@@ -60,6 +60,11 @@ def _load() -> C.CDLL:
         "spmm24_fwd_sparse_act": (i32, [sp, vp, i64, i64, vp, u32, vp, i64, vp]),
         "spmm24_bwd_dx": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, vp, vp]),
         "masked_dw_gemm": (i32, [vp, i64, vp, i64, i64, sp, vp, i64, vp]),
+        "spmm24_fwd_lowrank": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, i64, vp, u32, vp, i64, sp, vp]),
+        "spmm24_bwd_dx_lowrank": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, i64, vp, i64, vp, i64, vp, vp]),
+        "p24_gemm_nt": (i32, [vp, i64, i64, vp, i64, i64, i64, vp, i64, vp]),
+        "p24_gemm_tn": (i32, [vp, i64, vp, i64, i64, i64, i64, vp, i64, vp]),
+        "p24_transpose": (i32, [vp, i64, i64, i64, vp, i64, vp]),
         "p24_colsum_workspace_size": (sz, [i64, i64]),
         "p24_colsum": (i32, [vp, i64, i64, i64, vp, vp, sz, vp]),
         "p24_colsum_noalloc": (i32, [vp, i64, i64, i64, vp, vp]),
@@ -236,6 +241,76 @@ def spmm24_bwd_dx(dY: torch.Tensor, WbwdT: Sparse24, gate: torch.Tensor | None =
     _check(lib.spmm24_bwd_dx(dY.data_ptr(), M, lddy, C.byref(w), _ptr(gate), ldg, dX.data_ptr(), lddx,
                              _ptr(dbias), _stream(stream)), "spmm24_bwd_dx")
     return dX
+
+
+def spmm24_fwd_lowrank(X: torch.Tensor, W: Sparse24, T: torch.Tensor, L: torch.Tensor,
+                       bias: torch.Tensor | None = None, relu: bool = False, Y: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Y = act(X W^T + T L^T + bias): the sparse linear with SLOPE's low-rank adapter,
+    T = X R^T [M, r] (see p24_gemm_nt), L [N, r]."""
+    M, K, ldx = _mat(X, name="X")
+    N = W.rows
+    _, r, ldt = _mat(T, name="T")
+    _, _, ldl = _mat(L, name="L")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    _, _, ldy = _mat(Y, name="Y")
+    flags = (P24_EPI_BIAS if bias is not None else 0) | (P24_EPI_RELU if relu else 0)
+    w = W.c()
+    _check(lib.spmm24_fwd_lowrank(X.data_ptr(), M, ldx, C.byref(w), T.data_ptr(), ldt, L.data_ptr(), ldl, r,
+                                  _ptr(bias), flags, Y.data_ptr(), ldy, None, _stream(stream)), "spmm24_fwd_lowrank")
+    return Y
+
+
+def spmm24_bwd_dx_lowrank(dY: torch.Tensor, WbwdT: Sparse24, U: torch.Tensor, Rt: torch.Tensor,
+                          gate: torch.Tensor | None = None, dX: torch.Tensor | None = None,
+                          dbias: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dX = (dY W_bwd + U R) * [gate > 0]: U = dY L [M, r], Rt = R^T [K, r]."""
+    M, N, lddy = _mat(dY, name="dY")
+    K = WbwdT.rows
+    _, r, ldu = _mat(U, name="U")
+    _, _, ldrt = _mat(Rt, name="Rt")
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device) if dX is None else dX
+    _, _, lddx = _mat(dX, name="dX")
+    ldg = 0 if gate is None else _mat(gate, name="gate")[2]
+    w = WbwdT.c()
+    _check(lib.spmm24_bwd_dx_lowrank(dY.data_ptr(), M, lddy, C.byref(w), U.data_ptr(), ldu, Rt.data_ptr(), ldrt, r,
+                                     _ptr(gate), ldg, dX.data_ptr(), lddx, _ptr(dbias), _stream(stream)),
+           "spmm24_bwd_dx_lowrank")
+    return dX
+
+
+def p24_gemm_nt(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C = A B^T (bf16, fp32 accumulation): A [M, K], B [N, K]."""
+    M, K, lda = _mat(A, name="A")
+    N, K2, ldb = _mat(B, name="B")
+    if K2 != K:
+        raise ValueError("A and B need the same number of columns")
+    Cm = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if C_out is None else C_out
+    _, _, ldc = _mat(Cm, name="C")
+    _check(lib.p24_gemm_nt(A.data_ptr(), M, lda, B.data_ptr(), N, ldb, K, Cm.data_ptr(), ldc, _stream(stream)),
+           "p24_gemm_nt")
+    return Cm
+
+
+def p24_gemm_tn(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C = A^T B (contraction over the rows M): A [M, N], B [M, K] -> C [N, K]."""
+    M, N, lda = _mat(A, name="A")
+    M2, K, ldb = _mat(B, name="B")
+    if M2 != M:
+        raise ValueError("A and B need the same number of rows")
+    Cm = torch.empty((N, K), dtype=torch.bfloat16, device=A.device) if C_out is None else C_out
+    _, _, ldc = _mat(Cm, name="C")
+    _check(lib.p24_gemm_tn(A.data_ptr(), lda, B.data_ptr(), ldb, M, N, K, Cm.data_ptr(), ldc, _stream(stream)),
+           "p24_gemm_tn")
+    return Cm
+
+
+def p24_transpose(src: torch.Tensor, dst: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, cols, lds = _mat(src, name="src")
+    dst = torch.empty((cols, rows), dtype=torch.bfloat16, device=src.device) if dst is None else dst
+    _, _, ldd = _mat(dst, name="dst")
+    _check(lib.p24_transpose(src.data_ptr(), rows, cols, lds, dst.data_ptr(), ldd, _stream(stream)), "p24_transpose")
+    return dst
 
 
 def masked_dw_gemm(dY: torch.Tensor, X: torch.Tensor, Wfwd: Sparse24, dW: torch.Tensor | None = None,

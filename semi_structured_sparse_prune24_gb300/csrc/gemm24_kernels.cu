@@ -65,6 +65,7 @@ struct SpmmParams {
   int64_t a24_ldm;
   int* status;
   int b3d;  // B map is 3-D: {64 K, rows, K / 64}; one load brings both 64-K halves of a stage
+  int nad;  // dense stages per tile after the sparse ones: A_l [rowsA, r] . B_l [rowsB, r]^T, 64 of r each
 };
 
 struct DwParams {
@@ -169,6 +170,7 @@ struct SpmmSmem {
   static constexpr int kOffBar = kOffGate + 4 * BN * 4;
   static constexpr int kBytes = kOffBar + 8 * (3 * STAGES + 2 * kEBufs + 5) + 16;
   static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
+  static constexpr int kTxDense = 2 * (kA + kBHalf);  // a dense stage: A_l 128 x 64, B_l BN/2 x 64 per CTA
 };
 
 // TMEM column of the metadata of MMA j (0-3) of stage s: 8-column slots in the
@@ -209,6 +211,14 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tc_mma_sp_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t e_tmem,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -235,7 +245,8 @@ enum SpmmEpi : int {
 template <int BN, int STAGES, bool kTransOut, int kEpi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmE, const SpmmParams p) {
+                const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmL,
+                const __grid_constant__ CUtensorMap tmT, const SpmmParams p) {
   using L = SpmmSmem<BN, STAGES>;
   constexpr int kAccCols = 256;  // accumulator buffer b starts at column 256 * b
   // BN <= 192: two accumulator buffers (the epilogue of a tile overlaps the next
@@ -244,6 +255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   static_assert(BN <= 256 && BN % 16 == 0, "tile width");
   static_assert(kAccBufs == 1 ? 256 + 8 * 4 * STAGES <= 512 : 4 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
   constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, false);
+  constexpr uint32_t kIdescDense = idesc_bf16(2 * kBM, BN, /*sparse=*/false, false, false);
+  const int nstages = p.nkb + p.nad;  // per tile: sparse stages, then dense ones
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -281,6 +294,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmE);
+    if (p.nad) {
+      tma_prefetch_desc(&tmL);
+      tma_prefetch_desc(&tmT);
+    }
   }
   if (warp == 1) {  // pair allocation: one warp of each CTA, same columns in both
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -305,9 +322,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         int ta, tb;
         tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
         ta = 2 * ta + rank;
-        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+        for (int kb = 0; kb < nstages; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          if (kb >= p.nkb) {  // dense stage: 64 of the rank of A_l [rowsA, r] and B_l [rowsB, r]
+            if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+            if (leader) mbar_arrive_expect_tx(&full[s], L::kTxDense);
+            const uint32_t fullL = leader_addr(&full[s]);
+            const int j0 = (kb - p.nkb) * 64;
+            tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmL, fullL, j0, ta * kBM);
+            tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmT, fullL, j0, tb * BN + rank * (BN / 2));
+            continue;
+          }
           if (kb % kEStages == 0) {  // next metadata block
             const int e = eit % kEBufs;
             if (!p24_wait(&eempty[e], ((eit / kEBufs) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
@@ -351,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * kAccCols;
-        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+        for (int kb = 0; kb < nstages; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!p24_wait(&full[s], ph, abort_flag, p.status) ||
@@ -363,11 +389,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           if (lane == 0) {
             const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
             const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
+            if (kb < p.nkb) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t adesc = smem_desc(a_base + j * 32, 16, 1024, kSwizzle128B);
-              const uint64_t bdesc = smem_desc(b_base + (j >> 1) * L::kBHalf + (j & 1) * 64, 16, 1024, kSwizzle128B);
-              tc_mma_sp_pair(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
+              for (int j = 0; j < 4; ++j) {
+                const uint64_t adesc = smem_desc(a_base + j * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bdesc =
+                    smem_desc(b_base + (j >> 1) * L::kBHalf + (j & 1) * 64, 16, 1024, kSwizzle128B);
+                tc_mma_sp_pair(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
+              }
+            } else {  // dense stage: 4 x K=16 of the low-rank product, into the same accumulator
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint64_t adesc = smem_desc(a_base + j * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bdesc = smem_desc(b_base + j * 32, 16, 1024, kSwizzle128B);
+                tc_mma_pair(d_tmem, adesc, bdesc, kIdescDense, (kb | j) != 0);
+              }
             }
             tc_commit_pair(&empty[s], 0x3);
           }
@@ -400,9 +436,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       ta = 2 * ta + rank;
       const bool okA = ta * kBM + rowA < p.rowsA;
       const bool okB = ta * kBM + rowB < p.rowsA;
-      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+      for (int kb = 0; kb < nstages; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
+        if (kb >= p.nkb) {
+          // dense stage: no metadata; arrive once the slot is free, which keeps this
+          // barrier's phases in step with the stage ring
+          if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          __syncwarp();
+          if (lane == 0) arrive_cluster(leader_addr(&meta_ready[s]));
+          continue;
+        }
         const int eb_i = eit % kEBufs;
         if (kb % kEStages == 0 &&
             !p24_wait(&efull[eb_i], (eit / kEBufs) & 1, abort_flag, p.status)) { ok = false; break; }
@@ -602,7 +646,7 @@ struct DwSmem {
   static constexpr int kTx = kA + kB;
 };
 
-template <int STAGES>
+template <int STAGES, bool kMasked>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     dw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const DwParams p) {
   using L = DwSmem<STAGES>;
@@ -727,22 +771,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         tc_ld_32x32b_x32_wait(acc + c * 32, v);
         const int k0 = tb * BN + c * 32;
         if (row_ok && k0 < p.K) {
-          const int nbytes = min(4, (p.K - k0) / 8);  // 8 columns per metadata byte
-          uint32_t mw = 0;
-          const uint8_t* mrow = p.meta + static_cast<int64_t>(n) * p.ldm + k0 / 8;
-          if (nbytes == 4) mw = *reinterpret_cast<const uint32_t*>(mrow);
-          else
-            for (int i = 0; i < nbytes; ++i) mw |= static_cast<uint32_t>(mrow[i]) << (8 * i);
           uint32_t w[16];
+          if constexpr (kMasked) {
+            const int nbytes = min(4, (p.K - k0) / 8);  // 8 columns per metadata byte
+            uint32_t mw = 0;
+            const uint8_t* mrow = p.meta + static_cast<int64_t>(n) * p.ldm + k0 / 8;
+            if (nbytes == 4) mw = *reinterpret_cast<const uint32_t*>(mrow);
+            else
+              for (int i = 0; i < nbytes; ++i) mw |= static_cast<uint32_t>(mrow[i]) << (8 * i);
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t nib = (mw >> (4 * g)) & 0xFu;
-            const uint32_t kbits = (1u << (nib & 3u)) | (1u << (nib >> 2));
-            float f[4];
+            for (int g = 0; g < 8; ++g) {
+              const uint32_t nib = (mw >> (4 * g)) & 0xFu;
+              const uint32_t kbits = (1u << (nib & 3u)) | (1u << (nib >> 2));
+              float f[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) f[i] = (kbits >> i) & 1u ? __uint_as_float(v[4 * g + i]) : 0.f;
-            w[2 * g] = pack_bf16x2(f[0], f[1]);
-            w[2 * g + 1] = pack_bf16x2(f[2], f[3]);
+              for (int i = 0; i < 4; ++i) f[i] = (kbits >> i) & 1u ? __uint_as_float(v[4 * g + i]) : 0.f;
+              w[2 * g] = pack_bf16x2(f[0], f[1]);
+              w[2 * g + 1] = pack_bf16x2(f[2], f[3]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
           }
           __nv_bfloat16* o = p.out + static_cast<int64_t>(n) * p.ldo + k0;
 #pragma unroll
@@ -853,8 +902,8 @@ constexpr int kSpStages = 4;
 constexpr int kDwStages = 4;
 
 template <int BN, bool kTrans, int kEpi>
-cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const SpmmParams& p,
-                     cudaStream_t s) {
+cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const CUtensorMap& l,
+                     const CUtensorMap& t, const SpmmParams& p, cudaStream_t s) {
   using L = SpmmSmem<BN, kSpStages>;
   auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi>;
   const int smem = L::kBytes + 1024;
@@ -863,7 +912,7 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   int clusters = max_active_clusters(kern, 2, 320, smem);
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
-  kern<<<grid, 320, smem, s>>>(a, b, e, p);
+  kern<<<grid, 320, smem, s>>>(a, b, e, l, t, p);
   count_launch();
   return cudaGetLastError();
 }
@@ -916,18 +965,72 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  // low-rank term: dense stages after the sparse ones (a copy of A's map when there is none)
+  CUtensorMap tl = ta, tt = ta;
+  if (epi.lr_r > 0) {
+    if (!epi.lr_a || !epi.lr_b) return cudaErrorInvalidValue;
+    p.nad = static_cast<int>((epi.lr_r + 63) / 64);
+    if (!make_map_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, epi.lr_a, epi.lr_r, A.rows, epi.lr_lda * 2, 64, kBM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, epi.lr_b, epi.lr_r, rowsB, epi.lr_ldb * 2, 64, BN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   if (!transposed_out) {
     if (heavy_epilogue) return cudaErrorInvalidValue;  // the activation prune is transposed-only
-    return run_spmm<kSpBNWide, false, kEpiStore>(ta, tb, te, p, s);
+    return run_spmm<kSpBNWide, false, kEpiStore>(ta, tb, te, tl, tt, p, s);
   }
-  if (heavy_epilogue) return run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, p, s);
-  if (epi.gate || epi.dbias) return run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, p, s);
-  return run_spmm<kSpBNWide, true, kEpiStore>(ta, tb, te, p, s);
+  if (heavy_epilogue) return run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
+  if (epi.gate || epi.dbias) return run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
+  return run_spmm<kSpBNWide, true, kEpiStore>(ta, tb, te, tl, tt, p, s);
+}
+
+cudaError_t launch_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B, int64_t N, int64_t ldb, int64_t K,
+                           void* C, int64_t ldc, int* status, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  if (K == 0) return cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, s);
+  // the sparse GEMM's pipeline with only dense stages: A as the low-rank A_l, B as B_l
+  SpmmParams p{};
+  p.rowsA = static_cast<int>(M);
+  p.rowsB = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.tilesA = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
+  p.tilesB = static_cast<int>((N + kSpBNWide - 1) / kSpBNWide);
+  p.num_tiles = p.tilesA * p.tilesB;
+  p.group = std::min(p.tilesA, 16);
+  p.nkb = 0;
+  p.nad = static_cast<int>((K + 63) / 64);
+  p.out = static_cast<__nv_bfloat16*>(C);
+  p.ldo = ldc;
+  p.status = status;
+  CUtensorMap tl, tt;
+  if (!make_map_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, lda * 2, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&tt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, ldb * 2, 64, kSpBNWide / 2,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  return run_spmm<kSpBNWide, false, kEpiStore>(tl, tt, tl, tl, tt, p, s);
+}
+
+namespace {
+cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                   const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status, cudaStream_t s);
 }
 
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
                              int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
                              cudaStream_t s) {
+  if (!meta) return cudaErrorInvalidValue;
+  return run_dw(dY, lddy, X, ldx, M, N, K, meta, ldm, dW, lddw, status, s);
+}
+
+cudaError_t launch_gemm_tn(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                           void* C, int64_t ldc, int* status, cudaStream_t s) {
+  return run_dw(A, lda, B, ldb, M, N, K, nullptr, 0, C, ldc, status, s);
+}
+
+namespace {
+cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                   const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status, cudaStream_t s) {
   if (N == 0 || K == 0) return cudaSuccess;
   if (M == 0) {
     // empty reduction: dW = 0 everywhere
@@ -953,7 +1056,7 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
       !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   using L = DwSmem<kDwStages>;
-  auto kern = dw_kernel<kDwStages>;
+  auto kern = meta ? dw_kernel<kDwStages, true> : dw_kernel<kDwStages, false>;
   const int smem = L::kBytes + 1024;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -964,5 +1067,6 @@ cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_
   count_launch();
   return cudaGetLastError();
 }
+}  // namespace
 
 }  // namespace p24

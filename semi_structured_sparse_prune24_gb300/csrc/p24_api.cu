@@ -139,8 +139,24 @@ int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw
   return cuda_status(launch_compress_both(W, rows, cols, ldw, *fwd, *bwdT, W_masked, ldwm, as_stream(stream)));
 }
 
-int spmm24_fwd(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const float* bias, uint32_t flags,
-               void* Y, int64_t ldy, const p24_sparse* Y24, void* stream) {
+namespace {
+// the rank-r term of a low-rank call: rows of its two factors and their strides
+int check_lowrank(const void* a, int64_t rows_a, int64_t lda, const void* b, int64_t rows_b, int64_t ldb, int64_t r,
+                  p24::EpiArgs& epi) {
+  if (r <= 0 || r % 8 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(a, rows_a, r, lda));
+  P24_TRY(check_dense(b, rows_b, r, ldb));
+  if (rows_a > 0 && rows_b > 0 && (!a || !b)) return P24_EINVAL;
+  epi.lr_a = a;
+  epi.lr_lda = lda;
+  epi.lr_b = b;
+  epi.lr_ldb = ldb;
+  epi.lr_r = r;
+  return P24_OK;
+}
+
+int fwd_impl(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const float* bias, uint32_t flags, void* Y,
+             int64_t ldy, const p24_sparse* Y24, EpiArgs epi, void* stream) {
   if (flags & ~(P24_EPI_BIAS | P24_EPI_RELU | P24_EPI_ACT24)) return P24_EINVAL;
   P24_TRY(check_sparse(W));
   const int64_t N = W->rows, K = W->cols;
@@ -148,7 +164,6 @@ int spmm24_fwd(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const
   P24_TRY(check_dense(X, M, K, ldx));
   P24_TRY(check_dense(Y, M, N, ldy));
   if ((flags & P24_EPI_BIAS) && !bias) return P24_EINVAL;
-  EpiArgs epi;
   epi.bias = (flags & P24_EPI_BIAS) ? bias : nullptr;
   epi.relu = (flags & P24_EPI_RELU) != 0;
   if (flags & P24_EPI_ACT24) {
@@ -164,6 +179,21 @@ int spmm24_fwd(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const
   P24_TRY(cuda_status(launch_spmm(*W, X, M, ldx, Y, ldy, /*transposed_out=*/true, epi, st, s)));
   if (flags & P24_EPI_ACT24) return cuda_status(launch_pad(*Y24, s));
   return P24_OK;
+}
+}  // namespace
+
+int spmm24_fwd(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const float* bias, uint32_t flags,
+               void* Y, int64_t ldy, const p24_sparse* Y24, void* stream) {
+  return fwd_impl(X, M, ldx, W, bias, flags, Y, ldy, Y24, EpiArgs{}, stream);
+}
+
+int spmm24_fwd_lowrank(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const void* T, int64_t ldt,
+                       const void* L, int64_t ldl, int64_t r, const float* bias, uint32_t flags, void* Y, int64_t ldy,
+                       const p24_sparse* Y24, void* stream) {
+  P24_TRY(check_sparse(W));
+  EpiArgs epi;
+  P24_TRY(check_lowrank(L, W->rows, ldl, T, M, ldt, r, epi));
+  return fwd_impl(X, M, ldx, W, bias, flags, Y, ldy, Y24, epi, stream);
 }
 
 int spmm24_fwd_sparse_act(const p24_sparse* Xs, const void* Wm, int64_t N, int64_t ldw, const float* bias,
@@ -185,8 +215,9 @@ int spmm24_fwd_sparse_act(const p24_sparse* Xs, const void* Wm, int64_t N, int64
   return cuda_status(launch_spmm(*Xs, Wm, N, ldw, Y, ldy, /*transposed_out=*/false, epi, st, as_stream(stream)));
 }
 
-int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT, const void* gate, int64_t ldg,
-                  void* dX, int64_t lddx, float* dbias, void* stream) {
+namespace {
+int bwd_dx_impl(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT, const void* gate, int64_t ldg,
+                void* dX, int64_t lddx, float* dbias, EpiArgs epi, void* stream) {
   P24_TRY(check_sparse(WbwdT));
   const int64_t K = WbwdT->rows, N = WbwdT->cols;
   if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
@@ -198,13 +229,57 @@ int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* Wbw
   if (dbias) P24_TRY(cuda_status(cudaMemsetAsync(dbias, 0, K * 4, as_stream(stream))));
   if (M == 0) return P24_OK;
   if (N == 0) return P24_EUNSUPPORTED;
-  EpiArgs epi;
   epi.gate = gate;
   epi.ldg = ldg;
   epi.dbias = dbias;
   int* st = device_status_ptr();
   if (!st) return P24_ECUDA;
   return cuda_status(launch_spmm(*WbwdT, dY, M, lddy, dX, lddx, /*transposed_out=*/true, epi, st, as_stream(stream)));
+}
+}  // namespace
+
+int spmm24_bwd_dx(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT, const void* gate, int64_t ldg,
+                  void* dX, int64_t lddx, float* dbias, void* stream) {
+  return bwd_dx_impl(dY, M, lddy, WbwdT, gate, ldg, dX, lddx, dbias, EpiArgs{}, stream);
+}
+
+int spmm24_bwd_dx_lowrank(const void* dY, int64_t M, int64_t lddy, const p24_sparse* WbwdT, const void* U,
+                          int64_t ldu, const void* Rt, int64_t ldrt, int64_t r, const void* gate, int64_t ldg, void* dX,
+                          int64_t lddx, float* dbias, void* stream) {
+  P24_TRY(check_sparse(WbwdT));
+  EpiArgs epi;
+  P24_TRY(check_lowrank(Rt, WbwdT->rows, ldrt, U, M, ldu, r, epi));
+  return bwd_dx_impl(dY, M, lddy, WbwdT, gate, ldg, dX, lddx, dbias, epi, stream);
+}
+
+int p24_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B, int64_t N, int64_t ldb, int64_t K, void* C,
+                int64_t ldc, void* stream) {
+  if (K < 0) return P24_EINVAL;
+  P24_TRY(check_dense(A, M, K, lda));
+  P24_TRY(check_dense(B, N, K, ldb));
+  P24_TRY(check_dense(C, M, N, ldc));
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_gemm_nt(A, M, lda, B, N, ldb, K, C, ldc, st, as_stream(stream)));
+}
+
+int p24_gemm_tn(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M, int64_t N, int64_t K, void* C,
+                int64_t ldc, void* stream) {
+  P24_TRY(check_dense(A, M, N, lda));
+  P24_TRY(check_dense(B, M, K, ldb));
+  P24_TRY(check_dense(C, N, K, ldc));
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_gemm_tn(A, lda, B, ldb, M, N, K, C, ldc, st, as_stream(stream)));
+}
+
+int p24_transpose(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd, void* stream) {
+  // element-wise accesses: any stride and 2-byte alignment will do
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return P24_EINVAL;
+  if (rows == 0 || cols == 0) return P24_OK;
+  if (!src || !dst || lds < cols || ldd < rows) return P24_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 1) return P24_EALIGN;
+  return cuda_status(launch_transpose_bf16(src, rows, cols, lds, dst, ldd, as_stream(stream)));
 }
 
 int masked_dw_gemm(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, const p24_sparse* Wfwd,

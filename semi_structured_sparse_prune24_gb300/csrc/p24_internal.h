@@ -30,6 +30,12 @@ struct EpiArgs {
   const void* gate = nullptr;   // bf16 [M, ldg] ReLU output for the backward gate, or null
   int64_t ldg = 0;
   float* dbias = nullptr;              // += column sums of the stored output (transposed output only)
+  // low-rank term added to the product before the epilogue: lr_a [rows of A, r] . lr_b [rows of B, r]^T
+  const void* lr_a = nullptr;
+  int64_t lr_lda = 0;
+  const void* lr_b = nullptr;
+  int64_t lr_ldb = 0;
+  int64_t lr_r = 0;
   p24_sparse act24{};           // compressed activation output (vals != null => enabled)
 };
 
@@ -39,6 +45,15 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
                         int64_t ldo, bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s);
 
 // dW[n, k] = sum_m dY[m, n] * X[m, k] on mask(meta) (both operands MN-major).
+// C [M, N] = A [M, K] . B [N, K]^T, bf16 in and out, fp32 accumulation (K-major operands).
+cudaError_t launch_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B, int64_t N, int64_t ldb, int64_t K,
+                           void* C, int64_t ldc, int* status, cudaStream_t s);
+// C [N, K] = A [M, N]^T . B [M, K] (contraction over M), bf16 out, no mask.
+cudaError_t launch_gemm_tn(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                           void* C, int64_t ldc, int* status, cudaStream_t s);
+// dst [cols, rows] = src [rows, cols]^T, bf16.
+cudaError_t launch_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd,
+                                  cudaStream_t s);
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
                              int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
                              cudaStream_t s);

@@ -317,6 +317,36 @@ inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n 
 
 }  // namespace
 
+// dst [cols, rows] = src [rows, cols]^T for bf16: 32 x 32 tiles through shared
+// memory (one padding column against bank conflicts); coalesced on both sides.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ src, int64_t rows,
+                                                             int64_t cols, int64_t lds, uint16_t* __restrict__ dst,
+                                                             int64_t ldd) {
+  __shared__ uint16_t tile[32][33];
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32 threads
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + tx;
+    if (r < rows && c < cols) tile[i][tx] = src[r * lds + c];
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + tx;
+    if (c < cols && r < rows) dst[c * ldd + r] = tile[tx][i];
+  }
+}
+
+cudaError_t launch_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd,
+                                  cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if ((rows + 31) / 32 > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
+  transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src), rows, cols, lds,
+                                              static_cast<uint16_t*>(dst), ldd);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
   selftest_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
   count_launch();
