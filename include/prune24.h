@@ -283,6 +283,7 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
 /* Flags of ffn24_step. */
 #define P24_STEP_ACT24 0x1u /* 2:4-prune ReLU(up) and feed it as the sparse operand of down */
 #define P24_STEP_KEEP_MASKS 0x2u /* use the caller's compressed weights as they are (fixed masks) */
+#define P24_STEP_ADAPTERS 0x4u /* SLOPE's low-rank adapters on both linears (rank r) */
 
 /*
  * One FFN layer (up -> ReLU -> down), forward and backward, every matmul 2:4
@@ -312,6 +313,18 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
  *   With P24_STEP_KEEP_MASKS (fixed masks): the step reads them as they are,
  *   prunes nothing and does not read W_up / W_down (which may be NULL); the four
  *   compressed buffers (and W_down_masked under P24_STEP_ACT24) are required.
+ * Low-rank adapters (P24_STEP_ADAPTERS; see spmm24_fwd_lowrank): each linear
+ *   gains a dense rank-r term, the up one X R_up^T L_up^T and the down one
+ *   H R_down^T L_down^T, trained with exact gradients:
+ *   L_up [ffn, r], R_up [r, d], L_down [d, r], R_down [r, ffn] (bf16, contiguous)
+ *   and their gradients dL_up, dR_up, dL_down, dR_down of the same shapes:
+ *     T_up = X R_up^T;  H = ReLU(X W_up^T + T_up L_up^T + b_up);
+ *     T_dn = H R_down^T;  Y = H W_down^T + T_dn L_down^T + b_down;
+ *     U_dn = dY L_down;  dH = (dY W_down_bwd + U_dn R_down) * [H > 0];
+ *     U_up = dH L_up;  dX = dH W_up_bwd + U_up R_up;
+ *     dL_down = dY^T T_dn;  dR_down = U_dn^T H;  dL_up = dH^T T_up;  dR_up = U_up^T X
+ *   (T and U rounded to bf16). r > 0, r % 8 == 0; the workspace size then comes
+ *   from ffn24_workspace_size_lowrank.
  */
 typedef struct {
   int64_t M, d, ffn;
@@ -334,10 +347,21 @@ typedef struct {
   p24_sparse* down_fwd;
   p24_sparse* down_bwdT;
   void* W_down_masked;
+  int64_t r;
+  const void* L_up;
+  const void* R_up;
+  const void* L_down;
+  const void* R_down;
+  void* dL_up;
+  void* dR_up;
+  void* dL_down;
+  void* dR_down;
 } p24_ffn_args;
 
 /* Device workspace ffn24_step needs for these sizes (compressed weights, dH, ...). */
 size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags);
+/* The same with low-rank adapters of rank r (flags with P24_STEP_ADAPTERS). */
+size_t ffn24_workspace_size_lowrank(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r);
 int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream);
 
 /*

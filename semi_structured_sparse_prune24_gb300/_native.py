@@ -20,6 +20,7 @@ P24_OK, P24_EINVAL, P24_EALIGN, P24_ECUDA, P24_ETIMEOUT, P24_EUNSUPPORTED, P24_E
 P24_EPI_BIAS, P24_EPI_RELU, P24_EPI_ACT24 = 0x1, 0x2, 0x4
 P24_STEP_ACT24 = 0x1
 P24_STEP_KEEP_MASKS = 0x2
+P24_STEP_ADAPTERS = 0x4
 
 
 class P24Error(RuntimeError):
@@ -40,7 +41,9 @@ class p24_ffn_args(C.Structure):
                 ("dX", C.c_void_p), ("dW_up", C.c_void_p), ("dW_down", C.c_void_p), ("db_up", C.c_void_p),
                 ("db_down", C.c_void_p), ("up_fwd", C.POINTER(p24_sparse)), ("up_bwdT", C.POINTER(p24_sparse)),
                 ("down_fwd", C.POINTER(p24_sparse)), ("down_bwdT", C.POINTER(p24_sparse)),
-                ("W_down_masked", C.c_void_p)]
+                ("W_down_masked", C.c_void_p), ("r", C.c_int64), ("L_up", C.c_void_p), ("R_up", C.c_void_p),
+                ("L_down", C.c_void_p), ("R_down", C.c_void_p), ("dL_up", C.c_void_p), ("dR_up", C.c_void_p),
+                ("dL_down", C.c_void_p), ("dR_down", C.c_void_p)]
 
 
 def _load() -> C.CDLL:
@@ -69,6 +72,7 @@ def _load() -> C.CDLL:
         "p24_colsum": (i32, [vp, i64, i64, i64, vp, vp, sz, vp]),
         "p24_colsum_noalloc": (i32, [vp, i64, i64, i64, vp, vp]),
         "ffn24_workspace_size": (sz, [i64, i64, i64, u32]),
+        "ffn24_workspace_size_lowrank": (sz, [i64, i64, i64, u32, i64]),
         "ffn24_step": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp]),
         "ffn24_step_traced": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp, C.POINTER(vp), i32]),
         "p24_launch_count": (C.c_uint64, []),
@@ -347,6 +351,10 @@ def p24_colsum_noalloc(G: torch.Tensor, out: torch.Tensor | None = None, stream=
     return out
 
 
+def ffn24_workspace_size_lowrank(M: int, d: int, ffn: int, act24: bool, r: int) -> int:
+    return int(lib.ffn24_workspace_size_lowrank(M, d, ffn, (P24_STEP_ACT24 if act24 else 0) | P24_STEP_ADAPTERS, r))
+
+
 def ffn24_workspace_size(M: int, d: int, ffn: int, act24: bool = False) -> int:
     return int(lib.ffn24_workspace_size(M, d, ffn, P24_STEP_ACT24 if act24 else 0))
 
@@ -361,7 +369,7 @@ STEP_WEIGHTS = ("up_fwd", "up_bwdT", "down_fwd", "down_bwdT")
 
 def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict | None = None,
                workspace: torch.Tensor | None = None, stream=None, events=None, weights: dict | None = None,
-               keep_masks: bool = False) -> dict:
+               keep_masks: bool = False, adapters: dict | None = None) -> dict:
     """One 2:4 FFN layer fwd+bwd; returns dict(Y, H, dX, dW_up, dW_down, db_up, db_down).
 
     events: optional ctypes array of 2 * STEP_PHASES raw cudaEvent_t handles, recorded
@@ -370,7 +378,10 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     up_fwd [ffn, d], up_bwdT [d, ffn], down_fwd [d, ffn], down_bwdT [ffn, d] and a bf16
     W_down_masked [d, ffn]. Without keep_masks the step prunes W_up / W_down afresh and
     writes the results there; with keep_masks=True it uses them as they are (fixed
-    masks) and W_up / W_down are not read (they may be None)."""
+    masks) and W_up / W_down are not read (they may be None).
+    adapters: optional SLOPE low-rank adapters, a dict of bf16 tensors L_up [ffn, r],
+    R_up [r, d], L_down [d, r], R_down [r, ffn]; their gradients come back as
+    dL_up, dR_up, dL_down, dR_down (see include/prune24.h)."""
     M, d, _ = _mat(X, name="X")
     w = dict(weights or {})
     if keep_masks:
@@ -397,10 +408,19 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     o.setdefault("dW_down", torch.empty((d, ffn), dtype=bf, device=dev))
     o.setdefault("db_up", torch.empty(ffn, dtype=torch.float32, device=dev))
     o.setdefault("db_down", torch.empty(d, dtype=torch.float32, device=dev))
-    need = ffn24_workspace_size(M, d, ffn, act24)
+    r = 0
+    if adapters is not None:
+        r = adapters["L_up"].shape[1]
+        for k, shape in (("L_up", (ffn, r)), ("R_up", (r, d)), ("L_down", (d, r)), ("R_down", (r, ffn))):
+            t = adapters[k]
+            if t.dtype != bf or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"adapter {k} must be a contiguous bf16 {shape} tensor")
+            o.setdefault("d" + k, torch.empty(shape, dtype=bf, device=dev))
+    need = ffn24_workspace_size_lowrank(M, d, ffn, act24, r) if r else ffn24_workspace_size(M, d, ffn, act24)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    flags = (P24_STEP_ACT24 if act24 else 0) | (P24_STEP_KEEP_MASKS if keep_masks else 0)
+    flags = ((P24_STEP_ACT24 if act24 else 0) | (P24_STEP_KEEP_MASKS if keep_masks else 0) |
+             (P24_STEP_ADAPTERS if r else 0))
     a = p24_ffn_args(M, d, ffn, flags, X.data_ptr(), _ptr(W_up), _ptr(b_up),
                      _ptr(W_down), _ptr(b_down), dY.data_ptr(), o["Y"].data_ptr(), o["H"].data_ptr(),
                      o["dX"].data_ptr(), o["dW_up"].data_ptr(), o["dW_down"].data_ptr(), _ptr(o["db_up"]),
@@ -409,6 +429,11 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     for k, st in structs.items():
         setattr(a, k, C.pointer(st))
     a.W_down_masked = _ptr(w.get("W_down_masked"))
+    if r:
+        a.r = r
+        for k in ("L_up", "R_up", "L_down", "R_down"):
+            setattr(a, k, adapters[k].data_ptr())
+            setattr(a, "d" + k, o["d" + k].data_ptr())
     if events is None:
         _check(lib.ffn24_step(C.byref(a), workspace.data_ptr(), workspace.numel(), _stream(stream)), "ffn24_step")
     else:

@@ -53,11 +53,13 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of ffn24_step, carved in this order (each region 256-byte aligned).
 struct StepLayout {
   p24_sparse up_fwd, up_bwdT, dn_fwd, dn_bwdT, hs;
+  // low-rank adapters: T_up, T_dn, U_dn, U_up [M, r]; Lt_up [r, ffn], Lt_dn [r, d], Rt_up [d, r], Rt_dn [ffn, r]
+  void *T_up, *T_dn, *U_dn, *U_up, *Lt_up, *Lt_dn, *Rt_up, *Rt_dn;
   size_t off[16];
   size_t total;
 };
 
-void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, char* base, StepLayout& L,
+void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r, char* base, StepLayout& L,
                  void** wdm, void** dH, float** cs) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -85,6 +87,19 @@ void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, char* base, 
     *wdm = nullptr;
   }
   *dH = take(static_cast<size_t>(M * ffn * 2));
+  if ((flags & P24_STEP_ADAPTERS) && r > 0) {
+    const size_t mr = static_cast<size_t>(M * r * 2);
+    L.T_up = take(mr);
+    L.T_dn = take(mr);
+    L.U_dn = take(mr);
+    L.U_up = take(mr);
+    L.Lt_up = take(static_cast<size_t>(r * ffn * 2));
+    L.Lt_dn = take(static_cast<size_t>(r * d * 2));
+    L.Rt_up = take(static_cast<size_t>(d * r * 2));
+    L.Rt_dn = take(static_cast<size_t>(ffn * r * 2));
+  } else {
+    L.T_up = L.T_dn = L.U_dn = L.U_up = L.Lt_up = L.Lt_dn = L.Rt_up = L.Rt_dn = nullptr;
+  }
   const int64_t S = colsum_slabs(M);
   *cs = static_cast<float*>(take(static_cast<size_t>(S * (ffn > d ? ffn : d) * 4)));
   L.total = off;
@@ -322,13 +337,17 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
   return cuda_status(launch_colsum_noalloc(G, M, N, ldg, out, as_stream(stream)));
 }
 
-size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags) {
-  if (M < 0 || d < 0 || ffn < 0) return 0;
+size_t ffn24_workspace_size_lowrank(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r) {
+  if (M < 0 || d < 0 || ffn < 0 || r < 0) return 0;
   StepLayout L;
   void *wdm, *dH;
   float* cs;
-  step_layout(M, d, ffn, flags, nullptr, L, &wdm, &dH, &cs);
+  step_layout(M, d, ffn, flags, r, nullptr, L, &wdm, &dH, &cs);
   return L.total;
+}
+
+size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags) {
+  return ffn24_workspace_size_lowrank(M, d, ffn, flags, 0);
 }
 
 int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream) {
@@ -341,7 +360,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
                       int n_events) {
   if (!a) return P24_EINVAL;
   if (n_events < 0 || (n_events > 0 && !events)) return P24_EINVAL;
-  if (a->flags & ~(P24_STEP_ACT24 | P24_STEP_KEEP_MASKS)) return P24_EINVAL;
+  if (a->flags & ~(P24_STEP_ACT24 | P24_STEP_KEEP_MASKS | P24_STEP_ADAPTERS)) return P24_EINVAL;
   const int64_t M = a->M, d = a->d, ffn = a->ffn;
   if (M < 0 || d <= 0 || ffn <= 0 || d % 8 != 0 || ffn % 8 != 0) return P24_EINVAL;
   const bool act24 = (a->flags & P24_STEP_ACT24) != 0;
@@ -359,6 +378,19 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   }
   if (keep && act24 && !a->W_down_masked) return P24_EINVAL;
   if (a->W_down_masked) P24_TRY(check_dense(a->W_down_masked, d, ffn, ffn));
+  const bool ad = (a->flags & P24_STEP_ADAPTERS) != 0;
+  const int64_t r = a->r;
+  if (ad) {
+    if (r <= 0 || r % 8 != 0) return P24_EINVAL;
+    const void* in[4] = {a->L_up, a->R_up, a->L_down, a->R_down};
+    const void* out[4] = {a->dL_up, a->dR_up, a->dL_down, a->dR_down};
+    const int64_t rows[4] = {ffn, r, d, r}, cols[4] = {r, d, r, ffn};
+    for (int i = 0; i < 4; ++i) {
+      if (!in[i] || !out[i]) return P24_EINVAL;
+      P24_TRY(check_dense(in[i], rows[i], cols[i], cols[i]));
+      P24_TRY(check_dense(out[i], rows[i], cols[i], cols[i]));
+    }
+  }
   if (!keep) {
     P24_TRY(check_dense(a->W_up, ffn, d, d));
     P24_TRY(check_dense(a->W_down, d, ffn, ffn));
@@ -380,7 +412,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   StepLayout L;
   void *wdm, *dHv;
   float* cs;
-  step_layout(M, d, ffn, a->flags, static_cast<char*>(workspace), L, &wdm, &dHv, &cs);
+  step_layout(M, d, ffn, a->flags, ad ? r : 0, static_cast<char*>(workspace), L, &wdm, &dHv, &cs);
   if (ws_bytes < L.total) return P24_ENOSPACE;
   const cudaStream_t s = as_stream(stream);
   int* st = device_status_ptr();
@@ -405,15 +437,30 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   if (a->W_down_masked) wdm = a->W_down_masked;
   // 1. fresh 2:4 masks of both weights, and their double-pruned transposes (GMP);
   //    with fixed masks the caller's compressed weights are used as they are
+  //    (with adapters, also the transposed factors their backward products need)
   P24_PHASE(0, {
     if (!keep) P24_TRY(cuda_status(launch_compress_both(a->W_up, ffn, d, d, L.up_fwd, L.up_bwdT, nullptr, 0, s)));
+    if (ad) {
+      P24_TRY(cuda_status(launch_transpose_bf16(a->L_up, ffn, r, r, L.Lt_up, ffn, s)));
+      P24_TRY(cuda_status(launch_transpose_bf16(a->R_up, r, d, d, L.Rt_up, r, s)));
+    }
   });
   P24_PHASE(1, {
     if (!keep)
       P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT,
                                                (act24 || a->W_down_masked) ? wdm : nullptr, ffn, s)));
+    if (ad) {
+      P24_TRY(cuda_status(launch_transpose_bf16(a->L_down, d, r, r, L.Lt_dn, d, s)));
+      P24_TRY(cuda_status(launch_transpose_bf16(a->R_down, r, ffn, ffn, L.Rt_dn, r, s)));
+    }
   });
   if (M == 0) {
+    if (ad) {  // empty sums: zero adapter gradients
+      P24_TRY(cuda_status(cudaMemsetAsync(a->dL_up, 0, ffn * r * 2, s)));
+      P24_TRY(cuda_status(cudaMemsetAsync(a->dR_up, 0, r * d * 2, s)));
+      P24_TRY(cuda_status(cudaMemsetAsync(a->dL_down, 0, d * r * 2, s)));
+      P24_TRY(cuda_status(cudaMemsetAsync(a->dR_down, 0, r * ffn * 2, s)));
+    }
     if (a->db_up) P24_TRY(cuda_status(cudaMemsetAsync(a->db_up, 0, ffn * 4, s)));
     if (a->db_down) P24_TRY(cuda_status(cudaMemsetAsync(a->db_down, 0, d * 4, s)));
     P24_TRY(cuda_status(cudaMemsetAsync(a->dW_up, 0, ffn * d * 2, s)));
@@ -424,23 +471,37 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   up.bias = a->b_up;
   up.relu = true;
   if (act24) up.act24 = L.hs;
+  if (ad) {  // + T_up L_up^T, T_up = X R_up^T
+    up.lr_a = a->L_up, up.lr_lda = r, up.lr_b = L.T_up, up.lr_ldb = r, up.lr_r = r;
+  }
   P24_PHASE(2, {
+    if (ad) P24_TRY(cuda_status(launch_gemm_nt(a->X, M, d, a->R_up, r, d, d, L.T_up, r, st, s)));
     P24_TRY(cuda_status(launch_spmm(L.up_fwd, a->X, M, d, a->H, ffn, true, up, st, s)));
     if (act24) P24_TRY(cuda_status(launch_pad(L.hs, s)));
   });
   // 3. Y = H W_down^T + b_down
   EpiArgs dn;
   dn.bias = a->b_down;
-  if (act24)
-    P24_PHASE(3, P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s))));
-  else
-    P24_PHASE(3, P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s))));
+  if (ad) {  // + T_dn L_down^T, T_dn = H R_down^T (A and B swap roles in the sparse-activation form)
+    dn.lr_r = r;
+    if (act24) dn.lr_a = L.T_dn, dn.lr_lda = r, dn.lr_b = a->L_down, dn.lr_ldb = r;
+    else dn.lr_a = a->L_down, dn.lr_lda = r, dn.lr_b = L.T_dn, dn.lr_ldb = r;
+  }
+  P24_PHASE(3, {
+    if (ad) P24_TRY(cuda_status(launch_gemm_nt(a->H, M, ffn, a->R_down, r, ffn, ffn, L.T_dn, r, st, s)));
+    if (act24) P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s)));
+    else P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s)));
+  });
   // 4. dH = (dY W_down_bwd) * [H > 0], with db_up = column sums of dH fused into its epilogue
   EpiArgs g;
   g.gate = a->H;
   g.ldg = ffn;
   g.dbias = a->db_up;
+  if (ad) {  // + U_dn R_down, U_dn = dY L_down
+    g.lr_a = L.Rt_dn, g.lr_lda = r, g.lr_b = L.U_dn, g.lr_ldb = r, g.lr_r = r;
+  }
   P24_PHASE(4, {
+    if (ad) P24_TRY(cuda_status(launch_gemm_nt(a->dY, M, d, L.Lt_dn, r, d, d, L.U_dn, r, st, s)));
     if (a->db_up) P24_TRY(cuda_status(cudaMemsetAsync(a->db_up, 0, ffn * 4, s)));
     P24_TRY(cuda_status(launch_spmm(L.dn_bwdT, a->dY, M, d, dHv, ffn, true, g, st, s)));
   });
@@ -449,14 +510,32 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
     if (a->db_down) P24_TRY(cuda_status(launch_colsum(a->dY, M, d, d, a->db_down, cs, s)));
   });
   // 6. dW_down = (dY^T H) on mask(W_down)
-  P24_PHASE(6, P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm,
-                                                    a->dW_down, ffn, st, s))));
+  P24_PHASE(6, {
+    P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm, a->dW_down,
+                                         ffn, st, s)));
+    if (ad) {  // dL_down = dY^T T_dn, dR_down = U_dn^T H
+      P24_TRY(cuda_status(launch_gemm_tn(a->dY, d, L.T_dn, r, M, d, r, a->dL_down, r, st, s)));
+      P24_TRY(cuda_status(launch_gemm_tn(L.U_dn, r, a->H, ffn, M, r, ffn, a->dR_down, ffn, st, s)));
+    }
+  });
   // 7. dX = dH W_up_bwd
-  EpiArgs none;
-  P24_PHASE(7, P24_TRY(cuda_status(launch_spmm(L.up_bwdT, dHv, M, ffn, a->dX, d, true, none, st, s))));
+  EpiArgs gx;
+  if (ad) {  // + U_up R_up, U_up = dH L_up
+    gx.lr_a = L.Rt_up, gx.lr_lda = r, gx.lr_b = L.U_up, gx.lr_ldb = r, gx.lr_r = r;
+  }
+  P24_PHASE(7, {
+    if (ad) P24_TRY(cuda_status(launch_gemm_nt(dHv, M, ffn, L.Lt_up, r, ffn, ffn, L.U_up, r, st, s)));
+    P24_TRY(cuda_status(launch_spmm(L.up_bwdT, dHv, M, ffn, a->dX, d, true, gx, st, s)));
+  });
   // 8. dW_up = (dH^T X) on mask(W_up)
-  P24_PHASE(8, P24_TRY(cuda_status(
-                   launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s))));
+  P24_PHASE(8, {
+    P24_TRY(cuda_status(
+        launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s)));
+    if (ad) {  // dL_up = dH^T T_up, dR_up = U_up^T X
+      P24_TRY(cuda_status(launch_gemm_tn(dHv, ffn, L.T_up, r, M, ffn, r, a->dL_up, r, st, s)));
+      P24_TRY(cuda_status(launch_gemm_tn(L.U_up, r, a->X, d, M, r, d, a->dR_up, d, st, s)));
+    }
+  });
 #undef P24_PHASE
   return P24_OK;
 }

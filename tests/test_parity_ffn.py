@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from oracle import prune24_oracle as O
-from synth24 import WORKLOADS, FFNWorkload, ffn_inputs
+from synth24 import WORKLOADS, FFNWorkload, ffn_inputs, normal_bf16
 from tests.conftest import bits_of
 from tests.p24_testutil import assert_bits_equal, assert_close, propagated, sparse_bits, ulp_bf16
 
@@ -27,8 +27,9 @@ def P():
     return P
 
 
-def run_gpu(P, inp, act24):
-    o = P.ffn24_step(inp["X"], inp["W_up"], inp["b_up"], inp["W_down"], inp["b_down"], inp["dY"], act24=act24)
+def run_gpu(P, inp, act24, adapters=None):
+    o = P.ffn24_step(inp["X"], inp["W_up"], inp["b_up"], inp["W_down"], inp["b_down"], inp["dY"], act24=act24,
+                     adapters=adapters)
     torch.cuda.synchronize()
     assert P.p24_query_status() == 0
     return o
@@ -74,15 +75,18 @@ def disputed_positions(o, ref, w: FFNWorkload, act24: bool):
     return np.unique(ms), np.unique(fs), n
 
 
-def compare_step(o, ref, w: FFNWorkload, act24: bool):
+def compare_step(o, ref, w: FFNWorkload, act24: bool, adapters: dict | None = None):
     """Normwise on every output; elementwise everywhere except the rows/units a
     disputed rounded decision selects (see disputed_positions). Outputs computed
-    from a bf16 intermediate (H or dH) get the propagated-rounding term on top of
-    the elementwise bound: the two sides round that intermediate independently."""
+    from a bf16 intermediate (H or dH; with adapters also T and U) get the
+    propagated-rounding term on top of the elementwise bound: the two sides round
+    that intermediate independently, and the differences travel on."""
     ms, fs, _ = disputed_positions(o, ref, w, act24)
     km = np.setdiff1d(np.arange(w.M), ms)
     kf = np.setdiff1d(np.arange(w.ffn), fs)
     tm = lambda a: torch.as_tensor(a, device="cuda")  # noqa: E731
+    sq = lambda a: O.bf16_to_f32(a).astype(np.float32) ** 2  # noqa: E731
+    var = lambda bound: (bound / 4.0) ** 2  # noqa: E731  (a propagated 4-sigma bound back to a variance)
     uH2 = ulp_bf16(ref["H_used"]) ** 2                                   # [M, ffn]
     udH2 = ulp_bf16(ref["dH"]) ** 2                                      # [M, ffn]
     Wd2 = O.bf16_to_f32(O.decompress24(ref["down_vals"], ref["down_meta"], w.ffn)) ** 2      # [d, ffn]
@@ -90,12 +94,34 @@ def compare_step(o, ref, w: FFNWorkload, act24: bool):
     X2 = O.bf16_to_f32(ref["X"]) ** 2
     dY2 = O.bf16_to_f32(ref["dY"]) ** 2
     Hm = O.bf16_to_f32(ref["H_used"]) if act24 else ref["H_ref"]
-    assert_close(o["H"][tm(km)], Hm[km], "H")
-    assert_close(o["Y"][tm(km)], ref["Y_ref"][km], "Y", propagated(uH2[km], Wd2.T))
-    assert_close(o["dX"][tm(km)], ref["dX_ref"][km], "dX", propagated(udH2[km], WubT2.T))
+    eH = eY = edX = 0.0
+    if adapters is not None:
+        L_up2, R_up2, L_dn2, R_dn2 = (sq(adapters[k]) for k in ("L_up", "R_up", "L_down", "R_down"))
+        uTup2 = ulp_bf16(ref["T_up"]) ** 2                               # [M, r]
+        eH = propagated(uTup2, L_up2.T)                                  # H = ReLU(... + T_up L_up^T)
+        uH2 = uH2 + var(eH)
+        uTdn2 = ulp_bf16(ref["T_down"]) ** 2 + var(propagated(uH2, R_dn2.T))   # T_dn = H R_dn^T
+        uUdn2 = ulp_bf16(ref["U_down"]) ** 2                             # U_dn = dY L_dn
+        udH2 = udH2 + var(propagated(uUdn2, R_dn2))                      # dH gains U_dn R_dn
+        uUup2 = ulp_bf16(ref["U_up"]) ** 2 + var(propagated(udH2, L_up2))     # U_up = dH L_up
+        eY = propagated(uTdn2, L_dn2.T)
+        edX = propagated(uUup2, R_up2)
+    assert_close(o["H"][tm(km)], Hm[km], "H", eH[km] if adapters is not None else None)
+    assert_close(o["Y"][tm(km)], ref["Y_ref"][km], "Y", propagated(uH2[km], Wd2.T) + (eY[km] if adapters else 0))
+    assert_close(o["dX"][tm(km)], ref["dX_ref"][km], "dX",
+                 propagated(udH2[km], WubT2.T) + (edX[km] if adapters else 0))
     assert_close(o["dW_up"][tm(kf)], ref["dW_up_ref"][kf], "dW_up", propagated(udH2[:, kf].T, X2))
     assert_close(o["db_up"][tm(kf)], ref["db_up"][kf], "db_up", 4 * np.sqrt(udH2[:, kf].sum(0)))
     assert_close(o["dW_down"][:, tm(kf)], ref["dW_down_ref"][:, kf], "dW_down", propagated(dY2.T, uH2[:, kf]))
+    if adapters is not None:
+        Tup2, Tdn2, Udn2, Uup2 = (sq(ref[k]) for k in ("T_up", "T_down", "U_down", "U_up"))
+        H2, dH2 = sq(ref["H_used"]), sq(ref["dH"])
+        assert_close(o["dL_down"], ref["dL_down_ref"], "dL_down", propagated(dY2.T, uTdn2))
+        assert_close(o["dR_down"][:, tm(kf)], ref["dR_down_ref"][:, kf], "dR_down",
+                     (propagated(uUdn2.T, H2) + propagated(Udn2.T, uH2))[:, kf])
+        assert_close(o["dL_up"][tm(kf)], ref["dL_up_ref"][kf], "dL_up",
+                     propagated(udH2[:, kf].T, Tup2) + propagated(dH2[:, kf].T, uTup2))
+        assert_close(o["dR_up"], ref["dR_up_ref"], "dR_up", propagated(uUup2.T, X2))
     assert_close(o["db_down"], ref["db_down"], "db_down")
     for key in ("Y", "dX", "dW_up", "dW_down"):       # normwise over everything
         g = o[key].float().cpu().numpy().astype(np.float64)
@@ -106,9 +132,10 @@ def compare_step(o, ref, w: FFNWorkload, act24: bool):
     assert np.all(bits_of(o["dW_down"])[~O.mask_from_meta(ref["down_meta"], w.ffn)] == 0)
 
 
-def oracle_step(inp, act24):
+def oracle_step(inp, act24, adapters=None):
     r = O.ffn_step(bits_of(inp["X"]), bits_of(inp["W_up"]), inp["b_up"].cpu().numpy(), bits_of(inp["W_down"]),
-                   inp["b_down"].cpu().numpy(), bits_of(inp["dY"]), act24=act24)
+                   inp["b_down"].cpu().numpy(), bits_of(inp["dY"]), act24=act24,
+                   adapters=None if adapters is None else {k: bits_of(v) for k, v in adapters.items()})
     r["X"], r["dY"] = bits_of(inp["X"]), bits_of(inp["dY"])
     return r
 
@@ -301,3 +328,44 @@ def test_ffn_step_fixed_masks_against_the_oracle(P, act24):
     assert P.p24_query_status() == 0
     ref_inp = dict(inp, W_up=inp0["W_up"], W_down=inp0["W_down"])
     compare_step(o, oracle_step(ref_inp, act24), w, act24)
+
+
+def adapter_inputs(w: FFNWorkload, r: int, seed: int, ints: bool = False, device="cuda"):
+    """SLOPE adapters for a workload: L, R ~ N(0, 0.02^2) (tensor ids 10-13), or
+    integers in {-1, 0, 1} for the bit-exact test."""
+    from synth24 import small_int_bf16
+    shapes = {"L_up": (w.ffn, r), "R_up": (r, w.d), "L_down": (w.d, r), "R_down": (r, w.ffn)}
+    out = {}
+    for i, (k, shape) in enumerate(shapes.items()):
+        out[k] = (small_int_bf16(shape, -1, 1, seed, 10 + i, device) if ints
+                  else normal_bf16(shape, 0.02, seed, 10 + i, device))
+    return out
+
+
+@pytest.mark.parametrize("act24", [False, True])
+def test_ffn_step_adapters_integer_inputs_bit_exact(P, act24):
+    """Integer inputs and adapters: every fp32 sum of the step is an integer below
+    2**24, exact in any order, so every output (adapter gradients included) must agree
+    with the oracle bit for bit."""
+    w = FFNWorkload("int", 256, 264, 392, 1.0)
+    inp = integer_inputs(w, seed=5)
+    ad = adapter_inputs(w, 64, seed=5, ints=True)
+    o = run_gpu(P, inp, act24, ad)
+    ref = oracle_step(inp, act24, ad)
+    for k in ("H_ref", "Y_ref", "dH_ref", "dX_ref", "dW_up_ref", "dW_down_ref",
+              "dL_up_ref", "dR_up_ref", "dL_down_ref", "dR_down_ref"):
+        assert np.abs(ref[k]).max() < 2 ** 22, k
+    assert_bits_equal(bits_of(o["H"]), ref["H_used"] if act24 else ref["H"], "H")
+    for k in ("Y", "dX", "dW_up", "dW_down", "dL_up", "dR_up", "dL_down", "dR_down"):
+        assert_bits_equal(bits_of(o[k]), ref[k], k)
+    assert np.array_equal(o["db_up"].cpu().numpy(), ref["db_up"])
+    assert np.array_equal(o["db_down"].cpu().numpy(), ref["db_down"])
+
+
+@pytest.mark.parametrize("name,act24,r", [("gpt2", False, 64), ("gpt2", True, 64), ("1p3b", False, 128)])
+def test_ffn_step_adapters_workloads(P, name, act24, r):
+    w = WORKLOADS[name]
+    inp = ffn_inputs(w, seed=0, device="cuda", bias=False)
+    ad = adapter_inputs(w, r, seed=0)
+    o = run_gpu(P, inp, act24, ad)
+    compare_step(o, oracle_step(inp, act24, ad), w, act24, {k: bits_of(v) for k, v in ad.items()})
