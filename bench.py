@@ -286,6 +286,35 @@ def run_ours(args, world, rank, local):
                                (" x 2 (nominal 2:4 ratio)" if dk["peak"] == sparse_peak else "")
                                if dk["unit"] == "TFLOP/s" else f"{peak_src} hbm_gbs"}
 
+    # ---- the same step with SLOPE's low-rank adapters (rank 64) on both linears
+    slope = None
+    if not args.no_adapters:
+        r = 64
+        ad = {"L_up": normal_bf16((w.ffn, r), 0.02, seed, 10, dev), "R_up": normal_bf16((r, w.d), 0.02, seed, 11, dev),
+              "L_down": normal_bf16((w.d, r), 0.02, seed, 12, dev),
+              "R_down": normal_bf16((r, w.ffn), 0.02, seed, 13, dev)}
+        ws_ad = torch.empty(P.ffn24_workspace_size_lowrank(w.M, w.d, w.ffn, w.act24, r), dtype=torch.uint8,
+                            device=dev)
+        out_ad = P.ffn24_step(X, Wu, bu, Wd, bd, dY, act24=w.act24, workspace=ws_ad, adapters=ad)
+        for _ in range(args.warmup):
+            P.ffn24_step(X, Wu, bu, Wd, bd, dY, act24=w.act24, out=out_ad, workspace=ws_ad, adapters=ad)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a0.record(stream)
+        for _ in range(args.steps):
+            P.ffn24_step(X, Wu, bu, Wd, bd, dY, act24=w.act24, out=out_ad, workspace=ws_ad, adapters=ad)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        if P.p24_query_status() != 0:
+            raise RuntimeError("device status word set during the adapter steps")
+        ad_ms = a0.elapsed_time(a1) / args.steps
+        ad_flop = 12 * w.M * r * (w.d + w.ffn)  # T, term, U, dX term, dL, dR of both linears
+        slope = {"r": r, "ms_per_step": ad_ms, "value": (flop + ad_flop) / (ad_ms * 1e-3) / 1e12,
+                 "unit": "TFLOPS (dense-equivalent, adapter FLOPs included)", "adapter_flop": ad_flop,
+                 "overhead_vs_plain_step": ad_ms / ms_step - 1.0}
+        del out_ad, ws_ad, ad
+        torch.cuda.empty_cache()
+
     # ---- standalone prune of 1e9 bf16 ([31250, 32000]), HBM-bound
     prune = None
     if not args.no_prune:
@@ -369,6 +398,7 @@ def run_ours(args, world, rank, local):
             "phase_ms": dict(zip(P.STEP_PHASE_NAMES, phase_ms)),
             "kernels": breakdown,
             "roofline": roofline,
+            "slope_adapters": slope,
             "prune": prune,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -419,6 +449,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prune", action="store_true")
+    ap.add_argument("--no-adapters", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
