@@ -346,35 +346,38 @@ def run_ours(args, world, rank, local):
         hin = {k: v.cpu().pin_memory() for k, v in (("X", X), ("W_up", Wu), ("W_down", Wd), ("dY", dY))}
         hout = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory()
                 for k in ("Y", "dX", "dW_up", "dW_down", "db_up", "db_down")}
-        dX_, dWu_, dWd_, ddY_ = (torch.empty_like(t) for t in (X, Wu, Wd, dY))
         h2d = sum(t.numel() * t.element_size() for t in hin.values())
         d2h = sum(t.numel() * t.element_size() for t in hout.values())
-
-        def e2e_step():
-            dX_.copy_(hin["X"], non_blocking=True)
-            dWu_.copy_(hin["W_up"], non_blocking=True)
-            dWd_.copy_(hin["W_down"], non_blocking=True)
-            ddY_.copy_(hin["dY"], non_blocking=True)
-            P.ffn24_step(dX_, dWu_, bu, dWd_, bd, ddY_, act24=w.act24, out=out, workspace=ws)
-            for k, t in hout.items():
-                t.copy_(out[k], non_blocking=True)
-
+        # the package's StepPipeline: two device slots, copies on their own streams,
+        # overlapped with the previous / next step's compute
+        from semi_structured_sparse_prune24_gb300.pipeline import StepPipeline
+        del ws
+        torch.cuda.empty_cache()
+        pipe = StepPipeline(w.M, w.d, w.ffn, act24=w.act24, b_up=bu, b_down=bd, device=dev)
         for _ in range(args.warmup):
-            e2e_step()
+            pipe.submit(hin, hout)
+        pipe.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize(dev)
         e0.record(stream)
+        pipe.start_after(e0)
         for _ in range(args.steps):
-            e2e_step()
+            pipe.submit(hin, hout)
+        pipe.finish_on(stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
+        if P.p24_query_status() != 0:
+            raise RuntimeError("device status word set during the end-to-end steps")
         ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        del pipe
+        torch.cuda.empty_cache()
         e2e = {"value": world * flop / (ems * 1e-3) / 1e12, "unit": "TFLOPS (dense-equivalent)", "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "pinned host X, dY, W_up, W_down copied in and Y, dX, dW_up, dW_down, db copied out every "
-                       "step, on the step's stream"}
+                       "step through the package's StepPipeline (copy-in, compute and copy-out streams, two device "
+                       "slots: the copies of neighbouring steps overlap the compute)"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
