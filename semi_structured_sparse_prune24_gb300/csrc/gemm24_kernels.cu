@@ -76,6 +76,12 @@ struct DwParams {
   const uint8_t* meta;
   int64_t ldm;
   int* status;
+  // Extra tiles past the main ones, unmasked into out2: A-tile pairs >= tilesA_main read a
+  // second A operand (out2 rows 0..N2-1), B tiles >= tilesB_main a second B operand
+  // (out2 columns 0..K2-1). They share operand panels with the main tiles through L2.
+  int tilesA_main, tilesB_main, N2, K2;
+  __nv_bfloat16* out2;
+  int64_t ldo2;
 };
 
 // Grouped raster: consecutive tiles walk `group` A-tiles before the next
@@ -648,7 +654,8 @@ struct DwSmem {
 
 template <int STAGES, bool kMasked>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-    dw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const DwParams p) {
+    dw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, const DwParams p) {
   using L = DwSmem<STAGES>;
   constexpr int BN = 256;
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false, /*a_mn=*/true, /*b_mn=*/true);
@@ -678,6 +685,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.tilesA_main < p.tilesA) tma_prefetch_desc(&tmA2);
+    if (p.tilesB_main < p.tilesB) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -697,7 +706,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       for (int t = cid; t < p.num_tiles && ok; t += ncl) {
         int ta, tb;
         tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
-        ta = 2 * ta + rank;
+        // extra tiles read the second operands, from their first row / column
+        const bool xa = ta >= p.tilesA_main, xb = tb >= p.tilesB_main;
+        const CUtensorMap* ma = xa ? &tmA2 : &tmA;
+        const CUtensorMap* mb = xb ? &tmB2 : &tmB;
+        const int a0 = (2 * (xa ? ta - p.tilesA_main : ta) + rank) * kBM;
+        const int b0 = (xb ? tb - p.tilesB_main : tb) * BN;
         for (int kb = 0; kb < p.nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -705,9 +719,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full[s], L::kTx);
           uint8_t* a = smem + L::kOffA + s * L::kA;
           uint8_t* b = smem + L::kOffB + s * L::kB;
-          for (int i = 0; i < 2; ++i) tma_load_2d(a + i * 8192, &tmA, &full[s], ta * kBM + i * 64, kb * 64);
+          for (int i = 0; i < 2; ++i) tma_load_2d(a + i * 8192, ma, &full[s], a0 + i * 64, kb * 64);
           for (int i = 2 * rank; i < 2 * rank + 2; ++i)
-            tma_load_2d_mc(b + i * 8192, &tmB, &full[s], tb * BN + i * 64, kb * 64, 0x3);
+            tma_load_2d_mc(b + i * 8192, mb, &full[s], b0 + i * 64, kb * 64, 0x3);
         }
       }
       const uint32_t n_drain = it < STAGES ? it : STAGES;
@@ -758,12 +772,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     for (int t = cid; t < p.num_tiles; t += ncl, ++tl) {
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
-      ta = 2 * ta + rank;
+      const bool extra = ta >= p.tilesA_main || tb >= p.tilesB_main;
       const int b = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t acc = tmem + b * BN + (static_cast<uint32_t>(q * 32) << 16);
+      if (extra) {
+        // unmasked rows / columns of the second output
+        const int n2 = (2 * (ta >= p.tilesA_main ? ta - p.tilesA_main : ta) + rank) * kBM + q * 32 + lane;
+        const int kbase = (tb >= p.tilesB_main ? tb - p.tilesB_main : tb) * BN;
+        const int nlim = ta >= p.tilesA_main ? p.N2 : p.N;
+        const int klim = tb >= p.tilesB_main ? p.K2 : p.K;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32_wait(acc + c * 32, v);
+          const int k0 = kbase + c * 32;
+          if (n2 < nlim && k0 < klim) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+            __nv_bfloat16* o = p.out2 + static_cast<int64_t>(n2) * p.ldo2 + k0;
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc)
+              if (k0 + pc * 8 < klim)
+                *reinterpret_cast<uint4*>(o + pc * 8) = make_uint4(w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        continue;
+      }
+      ta = 2 * ta + rank;
       const int n = ta * kBM + q * 32 + lane;  // row of dW
       const bool row_ok = n < p.N;
       for (int c = 0; c < BN / 32; ++c) {
@@ -1013,47 +1054,78 @@ cudaError_t launch_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B,
 
 namespace {
 cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N, int64_t K,
-                   const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status, cudaStream_t s);
+                   const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, const DwExtra& ex, int* status,
+                   cudaStream_t s);
 }
 
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
                              int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
                              cudaStream_t s) {
   if (!meta) return cudaErrorInvalidValue;
-  return run_dw(dY, lddy, X, ldx, M, N, K, meta, ldm, dW, lddw, status, s);
+  return run_dw(dY, lddy, X, ldx, M, N, K, meta, ldm, dW, lddw, DwExtra{}, status, s);
+}
+
+cudaError_t launch_masked_dw_extra(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
+                                   int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw,
+                                   const DwExtra& ex, int* status, cudaStream_t s) {
+  if (!meta || !ex.out2 || (ex.a2 != nullptr) == (ex.b2 != nullptr)) return cudaErrorInvalidValue;
+  return run_dw(dY, lddy, X, ldx, M, N, K, meta, ldm, dW, lddw, ex, status, s);
 }
 
 cudaError_t launch_gemm_tn(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M, int64_t N, int64_t K,
                            void* C, int64_t ldc, int* status, cudaStream_t s) {
-  return run_dw(A, lda, B, ldb, M, N, K, nullptr, 0, C, ldc, status, s);
+  return run_dw(A, lda, B, ldb, M, N, K, nullptr, 0, C, ldc, DwExtra{}, status, s);
 }
 
 namespace {
 cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N, int64_t K,
-                   const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status, cudaStream_t s) {
+                   const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, const DwExtra& ex, int* status,
+                   cudaStream_t s) {
   if (N == 0 || K == 0) return cudaSuccess;
   if (M == 0) {
     // empty reduction: dW = 0 everywhere
+    if (ex.a2 && ex.n2 > 0) {
+      cudaError_t e = cudaMemset2DAsync(ex.out2, ex.ldo2 * 2, 0, K * 2, ex.n2, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (ex.b2 && ex.k2 > 0) {
+      cudaError_t e = cudaMemset2DAsync(ex.out2, ex.ldo2 * 2, 0, ex.k2 * 2, N, s);
+      if (e != cudaSuccess) return e;
+    }
     return cudaMemset2DAsync(dW, lddw * 2, 0, K * 2, N, s);
   }
   DwParams p{};
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.M = static_cast<int>(M);
-  p.tilesA = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));  // A tile pairs (one per cluster)
-  p.tilesB = static_cast<int>((K + 255) / 256);
+  p.tilesA_main = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));  // A tile pairs (one per cluster)
+  p.tilesB_main = static_cast<int>((K + 255) / 256);
+  p.tilesA = p.tilesA_main + (ex.a2 ? static_cast<int>((ex.n2 + 2 * kBM - 1) / (2 * kBM)) : 0);
+  p.tilesB = p.tilesB_main + (ex.b2 ? static_cast<int>((ex.k2 + 255) / 256) : 0);
   p.num_tiles = p.tilesA * p.tilesB;
-  p.group = std::min(p.tilesA, 8);
+  // groups of at most 8 A-tile pairs, evened out so that extra A tiles join main ones
+  p.group = (p.tilesA + (p.tilesA + 7) / 8 - 1) / ((p.tilesA + 7) / 8);
   p.nkb = static_cast<int>((M + 63) / 64);
   p.out = static_cast<__nv_bfloat16*>(dW);
   p.ldo = lddw;
   p.meta = meta;
   p.ldm = ldm;
   p.status = status;
-  CUtensorMap ta, tb;
+  p.N2 = static_cast<int>(ex.n2);
+  p.K2 = static_cast<int>(ex.k2);
+  p.out2 = static_cast<__nv_bfloat16*>(ex.out2);
+  p.ldo2 = ex.ldo2;
+  CUtensorMap ta, tb, ta2, tb2;
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dY, N, M, lddy * 2, 64, 64,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  ta2 = ta;
+  tb2 = tb;
+  if ((ex.a2 && !make_map_2d(&ta2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ex.a2, ex.n2, M, ex.lda2 * 2, 64, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B)) ||
+      (ex.b2 && !make_map_2d(&tb2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ex.b2, ex.k2, M, ex.ldb2 * 2, 64, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B)))
     return cudaErrorInvalidValue;
   using L = DwSmem<kDwStages>;
   auto kern = meta ? dw_kernel<kDwStages, true> : dw_kernel<kDwStages, false>;
@@ -1063,7 +1135,7 @@ cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int
   int clusters = max_active_clusters(kern, 2, 192, smem);
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
-  kern<<<grid, 192, smem, s>>>(ta, tb, p);
+  kern<<<grid, 192, smem, s>>>(ta, tb, ta2, tb2, p);
   count_launch();
   return cudaGetLastError();
 }

@@ -511,11 +511,19 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   });
   // 6. dW_down = (dY^T H) on mask(W_down)
   P24_PHASE(6, {
-    P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm, a->dW_down,
-                                         ffn, st, s)));
-    if (ad) {  // dL_down = dY^T T_dn, dR_down = U_dn^T H
+    if (ad) {  // dR_down = U_dn^T H as extra rows of the same pass over H; dL_down = dY^T T_dn
+      DwExtra ex;
+      ex.a2 = L.U_dn;
+      ex.lda2 = r;
+      ex.n2 = r;
+      ex.out2 = a->dR_down;
+      ex.ldo2 = ffn;
+      P24_TRY(cuda_status(launch_masked_dw_extra(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm,
+                                                 a->dW_down, ffn, ex, st, s)));
       P24_TRY(cuda_status(launch_gemm_tn(a->dY, d, L.T_dn, r, M, d, r, a->dL_down, r, st, s)));
-      P24_TRY(cuda_status(launch_gemm_tn(L.U_dn, r, a->H, ffn, M, r, ffn, a->dR_down, ffn, st, s)));
+    } else {
+      P24_TRY(cuda_status(launch_masked_dw(a->dY, d, a->H, ffn, M, d, ffn, L.dn_fwd.meta, L.dn_fwd.ldm, a->dW_down,
+                                           ffn, st, s)));
     }
   });
   // 7. dX = dH W_up_bwd
@@ -529,11 +537,19 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   });
   // 8. dW_up = (dH^T X) on mask(W_up)
   P24_PHASE(8, {
-    P24_TRY(cuda_status(
-        launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s)));
-    if (ad) {  // dL_up = dH^T T_up, dR_up = U_up^T X
-      P24_TRY(cuda_status(launch_gemm_tn(dHv, ffn, L.T_up, r, M, ffn, r, a->dL_up, r, st, s)));
+    if (ad) {  // dL_up = dH^T T_up as extra columns of the same pass over dH; dR_up = U_up^T X
+      DwExtra ex;
+      ex.b2 = L.T_up;
+      ex.ldb2 = r;
+      ex.k2 = r;
+      ex.out2 = a->dL_up;
+      ex.ldo2 = r;
+      P24_TRY(cuda_status(launch_masked_dw_extra(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm,
+                                                 a->dW_up, d, ex, st, s)));
       P24_TRY(cuda_status(launch_gemm_tn(L.U_up, r, a->X, d, M, r, d, a->dR_up, d, st, s)));
+    } else {
+      P24_TRY(cuda_status(
+          launch_masked_dw(dHv, ffn, a->X, d, M, ffn, d, L.up_fwd.meta, L.up_fwd.ldm, a->dW_up, d, st, s)));
     }
   });
 #undef P24_PHASE

@@ -54,6 +54,20 @@ cudaError_t launch_gemm_tn(const void* A, int64_t lda, const void* B, int64_t ld
 // dst [cols, rows] = src [rows, cols]^T, bf16.
 cudaError_t launch_transpose_bf16(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd,
                                   cudaStream_t s);
+// Extra output of a masked dW launch, computed unmasked from the same pass: a second
+// A operand a2 [M, n2] gives out2 [n2, K] = a2^T . X (it shares X's panels), or a second
+// B operand b2 [M, k2] gives out2 [N, k2] = dY^T . b2 (it shares dY's panels).
+struct DwExtra {
+  const void* a2 = nullptr;
+  int64_t lda2 = 0, n2 = 0;
+  const void* b2 = nullptr;
+  int64_t ldb2 = 0, k2 = 0;
+  void* out2 = nullptr;
+  int64_t ldo2 = 0;
+};
+cudaError_t launch_masked_dw_extra(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
+                                   int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw,
+                                   const DwExtra& ex, int* status, cudaStream_t s);
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
                              int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
                              cudaStream_t s);
