@@ -315,6 +315,42 @@ def run_ours(args, world, rank, local):
         del out_ad, ws_ad, ad
         torch.cuda.empty_cache()
 
+    # ---- a short step (GPT-2-size FFN), eager against a CUDA-graph replay: the
+    #      per-launch host work that a graph removes
+    graphs = None
+    if not args.no_graphs:
+        from semi_structured_sparse_prune24_gb300.graph import StepGraph
+        from synth24 import ffn_inputs
+        ws_small = WORKLOADS["gpt2"]
+        small = ffn_inputs(ws_small, seed=seed, device=dev, bias=True)
+        g = StepGraph(small, act24=False)
+        n_rep = 50
+
+        def timed(fn):
+            for _ in range(5):
+                fn()
+            t0_, t1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            t0_.record(g.stream)
+            for _ in range(n_rep):
+                fn()
+            t1_.record(g.stream)
+            torch.cuda.synchronize(dev)
+            return t0_.elapsed_time(t1_) / n_rep
+
+        ws_e = torch.empty(P.ffn24_workspace_size(ws_small.M, ws_small.d, ws_small.ffn), dtype=torch.uint8, device=dev)
+        eager_out = P.ffn24_step(small["X"], small["W_up"], small["b_up"], small["W_down"], small["b_down"],
+                                 small["dY"], workspace=ws_e, stream=g.stream)
+        eager_ms = timed(lambda: P.ffn24_step(small["X"], small["W_up"], small["b_up"], small["W_down"], small["b_down"],
+                                              small["dY"], out=eager_out, workspace=ws_e, stream=g.stream))
+        graph_ms = timed(g.replay)
+        graphs = {"workload": ws_small.name, "eager_ms_per_step": eager_ms, "graph_ms_per_step": graph_ms,
+                  "graph_value": ws_small.dense_equiv_flop / (graph_ms * 1e-3) / 1e12,
+                  "eager_value": ws_small.dense_equiv_flop / (eager_ms * 1e-3) / 1e12,
+                  "unit": "TFLOPS (dense-equivalent)", "note": "back-to-back steps on resident inputs, L2-warm"}
+        del g, small, eager_out, ws_e
+        torch.cuda.empty_cache()
+
     # ---- standalone prune of 1e9 bf16 ([31250, 32000]), HBM-bound
     prune = None
     if not args.no_prune:
@@ -402,6 +438,7 @@ def run_ours(args, world, rank, local):
             "kernels": breakdown,
             "roofline": roofline,
             "slope_adapters": slope,
+            "graphs": graphs,
             "prune": prune,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -453,6 +490,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prune", action="store_true")
     ap.add_argument("--no-adapters", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
