@@ -196,7 +196,7 @@ def cpu_baseline(w, seconds_target: float = 15.0) -> dict:
 # ------------------------------------------------------------------ our arm
 def run_ours(args, world, rank, local):
     import semi_structured_sparse_prune24_gb300 as P
-    from synth24 import WORKLOADS, normal_bf16
+    from synth24 import WORKLOADS, ffn_inputs, normal_bf16
 
     w = WORKLOADS[args.workload]
     torch.cuda.set_device(local)
@@ -320,7 +320,6 @@ def run_ours(args, world, rank, local):
     graphs = None
     if not args.no_graphs:
         from semi_structured_sparse_prune24_gb300.graph import StepGraph
-        from synth24 import ffn_inputs
         ws_small = WORKLOADS["gpt2"]
         small = ffn_inputs(ws_small, seed=seed, device=dev, bias=True)
         g = StepGraph(small, act24=False)
@@ -349,6 +348,60 @@ def run_ours(args, world, rank, local):
                   "eager_value": ws_small.dense_equiv_flop / (eager_ms * 1e-3) / 1e12,
                   "unit": "TFLOPS (dense-equivalent)", "note": "back-to-back steps on resident inputs, L2-warm"}
         del g, small, eager_out, ws_e
+        torch.cuda.empty_cache()
+
+    # ---- the other configurations, one GPU each (inputs resident, same timing)
+    configs = None
+    if not args.no_sweep:
+        configs = {}
+
+        def time_calls(fn):
+            for _ in range(args.warmup):
+                fn()
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            c0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            c1.record(stream)
+            torch.cuda.synchronize(dev)
+            return c0.elapsed_time(c1) / args.steps
+
+        for key in ("gpt2", "1p3b", "7b_act24", "70b_m2048", "70b_m8192"):
+            cw = WORKLOADS[key]
+            ci = ffn_inputs(cw, seed=seed, device=dev, bias=False)
+            cws = torch.empty(P.ffn24_workspace_size(cw.M, cw.d, cw.ffn, cw.act24), dtype=torch.uint8, device=dev)
+            co = P.ffn24_step(ci["X"], ci["W_up"], ci["b_up"], ci["W_down"], ci["b_down"], ci["dY"], act24=cw.act24,
+                              workspace=cws)
+            cms = time_calls(lambda: P.ffn24_step(ci["X"], ci["W_up"], ci["b_up"], ci["W_down"], ci["b_down"], ci["dY"],
+                                                  act24=cw.act24, out=co, workspace=cws))
+            cv = cw.dense_equiv_flop / (cms * 1e-3) / 1e12
+            configs[cw.name] = {"ms_per_step": cms, "value": cv, "pct_sparse_peak": cv / sparse_peak,
+                                "dense_equiv_flop": cw.dense_equiv_flop}
+            del ci, cws, co
+        # single linears (prune + forward + double-pruned dX + masked dW): the 70B tail
+        # shape and the tiny check
+        for name, (lm, ln, lk) in (("ffn_70b_tail_linear_M1000_K8200_N28672", (1000, 28672, 8200)),
+                                   ("tiny_single_linear_N256_K512_M128", (128, 256, 512))):
+            lx = normal_bf16((lm, lk), 1.0, seed, 1, dev)
+            lw = normal_bf16((ln, lk), 0.01, seed, 2, dev)
+            ldy = normal_bf16((lm, ln), 1.0, seed, 6, dev)
+            fwd, bwdT = P.Sparse24.empty(ln, lk, dev), P.Sparse24.empty(lk, ln, dev)
+            ly = torch.empty((lm, ln), dtype=torch.bfloat16, device=dev)
+            ldx = torch.empty((lm, lk), dtype=torch.bfloat16, device=dev)
+            ldw = torch.empty((ln, lk), dtype=torch.bfloat16, device=dev)
+
+            def linear_step():
+                P.prune24_compress_both(lw, fwd, bwdT)
+                P.spmm24_fwd(lx, fwd, Y=ly)
+                P.spmm24_bwd_dx(ldy, bwdT, dX=ldx)
+                P.masked_dw_gemm(ldy, lx, fwd, dW=ldw)
+            lms = time_calls(linear_step)
+            lf = 6 * lm * ln * lk
+            lv = lf / (lms * 1e-3) / 1e12
+            configs[name] = {"ms_per_step": lms, "value": lv, "pct_sparse_peak": lv / sparse_peak,
+                             "dense_equiv_flop": lf}
+            del lx, lw, ldy, fwd, bwdT, ly, ldx, ldw
         torch.cuda.empty_cache()
 
     # ---- standalone prune of 1e9 bf16 ([31250, 32000]), HBM-bound
@@ -439,6 +492,7 @@ def run_ours(args, world, rank, local):
             "roofline": roofline,
             "slope_adapters": slope,
             "graphs": graphs,
+            "configs": configs,
             "prune": prune,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -491,6 +545,7 @@ def main():
     ap.add_argument("--no-prune", action="store_true")
     ap.add_argument("--no-adapters", action="store_true")
     ap.add_argument("--no-graphs", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
