@@ -904,6 +904,8 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
 // Clusters of `cluster` CTAs of this kernel that can be resident at once (GPCs
 // need not divide evenly into clusters, so this can be below SMs / cluster).
 // A persistent grid larger than this would leave whole clusters for a second wave.
+constexpr int kMaxDevices = 64;
+
 template <class Kern>
 int max_active_clusters(Kern kern, int cluster, int threads, int smem) {
   cudaLaunchConfig_t cfg = {};
@@ -923,6 +925,27 @@ int max_active_clusters(Kern kern, int cluster, int threads, int smem) {
     return 0;
   }
   return n;
+}
+
+// Per-device launch setup of one kernel instantiation: its dynamic shared memory
+// attribute set once, and the number of co-resident clusters (0: query failed, use
+// SMs / 2). Kept per device, computed on the first launch there.
+struct LaunchSetup {
+  std::once_flag once[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+  int clusters[kMaxDevices] = {};
+};
+
+template <class Kern>
+cudaError_t launch_setup(LaunchSetup& ls, Kern kern, int cluster, int threads, int smem, int& clusters) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(ls.once[dev], [&] {
+    ls.err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (ls.err[dev] == cudaSuccess) ls.clusters[dev] = max_active_clusters(kern, cluster, threads, smem);
+  });
+  clusters = ls.clusters[dev];
+  return ls.err[dev];
 }
 
 int num_sms() {
@@ -948,9 +971,10 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   using L = SpmmSmem<BN, kSpStages>;
   auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi>;
   const int smem = L::kBytes + 1024;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static LaunchSetup setup;
+  int clusters = 0;
+  cudaError_t err = launch_setup(setup, kern, 2, 320, smem, clusters);
   if (err != cudaSuccess) return err;
-  int clusters = max_active_clusters(kern, 2, 320, smem);
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
   kern<<<grid, 320, smem, s>>>(a, b, e, l, t, p);
@@ -1130,9 +1154,10 @@ cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int
   using L = DwSmem<kDwStages>;
   auto kern = meta ? dw_kernel<kDwStages, true> : dw_kernel<kDwStages, false>;
   const int smem = L::kBytes + 1024;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static LaunchSetup setup_masked, setup_plain;
+  int clusters = 0;
+  cudaError_t err = launch_setup(meta ? setup_masked : setup_plain, kern, 2, 192, smem, clusters);
   if (err != cudaSuccess) return err;
-  int clusters = max_active_clusters(kern, 2, 192, smem);
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
   kern<<<grid, 192, smem, s>>>(ta, tb, ta2, tb2, p);

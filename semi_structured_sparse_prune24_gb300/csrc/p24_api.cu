@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <mutex>
 #include <cstdint>
 #include <cstring>
 
@@ -111,9 +112,17 @@ std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int* device_status_ptr() {
-  int* p = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status) != cudaSuccess) return nullptr;
-  return p;
+  // the status word's device address, looked up once per device
+  constexpr int kDevs = 64;
+  static std::once_flag once[kDevs];
+  static int* addr[kDevs] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return nullptr;
+  std::call_once(once[dev], [dev] {
+    int* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status) == cudaSuccess) addr[dev] = p;
+  });
+  return addr[dev];
 }
 
 }  // namespace p24
