@@ -460,10 +460,24 @@ def run_ours(args, world, rank, local):
         if P.p24_query_status() != 0:
             raise RuntimeError("device status word set during the end-to-end steps")
         ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        # the copies alone, each direction on its own (what the overlap has to hide)
+        def copy_ms(fn, s_):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            c0.record(s_)
+            with torch.cuda.stream(s_):
+                fn()
+            c1.record(s_)
+            torch.cuda.synchronize(dev)
+            return c0.elapsed_time(c1)
+        cin = copy_ms(lambda: [pipe.inputs[0][k].copy_(hin[k], non_blocking=True) for k in hin], pipe.s_in)
+        cout = copy_ms(lambda: [hout[k].copy_(pipe.outputs[0][k], non_blocking=True) for k in hout], pipe.s_out)
         del pipe
         torch.cuda.empty_cache()
         e2e = {"value": world * flop / (ems * 1e-3) / 1e12, "unit": "TFLOPS (dense-equivalent)", "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "copy_in_ms_alone": cin, "copy_out_ms_alone": cout,
+               "copy_in_gbs": h2d / (cin * 1e-3) / 1e9, "copy_out_gbs": d2h / (cout * 1e-3) / 1e9,
                "note": "pinned host X, dY, W_up, W_down copied in and Y, dX, dW_up, dW_down, db copied out every "
                        "step through the package's StepPipeline (copy-in, compute and copy-out streams, two device "
                        "slots: the copies of neighbouring steps overlap the compute)"}
