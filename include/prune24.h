@@ -125,6 +125,10 @@ int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw
 #define P24_EPI_BIAS  0x1u  /* add an fp32 bias per output column */
 #define P24_EPI_RELU  0x2u  /* ReLU after the bias (sets +0 for x <= 0) */
 #define P24_EPI_ACT24 0x4u  /* 2:4-prune the bf16 output along its columns */
+/* Test only (spmm24_fwd): the first CTA pair skips the loads of one pipeline stage,
+ * so that the bounded waits of the real kernel expire; the call then leaves
+ * P24_ETIMEOUT in the status word (see p24_query_timeout) and Y undefined. */
+#define P24_EPI_TEST_STALL 0x80000000u
 
 /*
  * spmm24_fwd -- forward linear with a 2:4 weight on the sparse tensor cores
@@ -397,6 +401,15 @@ int p24_query_status(void* stream);
  * clears it); the context stays usable. Nothing is faulted, trapped or hung.
  */
 int p24_selftest_timeout(int64_t limit_ns, void* stream);
+
+/*
+ * p24_query_timeout -- p24_query_status that also reports where the first
+ * expired wait happened: *cta = its CTA (blockIdx.x) and *barrier = the shared
+ * memory address of the mbarrier it waited on, as that CTA saw it (the offset in
+ * the low 24 bits; a CTA of a cluster has its rank above them). Both are -1 when
+ * the status is P24_OK. Either pointer may be NULL. Clears the status.
+ */
+int p24_query_timeout(void* stream, int64_t* cta, int64_t* barrier);
 
 /* Static text for a p24_status code. */
 const char* p24_strerror(int code);

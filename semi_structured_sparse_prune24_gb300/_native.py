@@ -18,6 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 P24_OK, P24_EINVAL, P24_EALIGN, P24_ECUDA, P24_ETIMEOUT, P24_EUNSUPPORTED, P24_ENOSPACE = 0, -1, -2, -3, -4, -5, -6
 P24_EPI_BIAS, P24_EPI_RELU, P24_EPI_ACT24 = 0x1, 0x2, 0x4
+P24_EPI_TEST_STALL = 0x80000000
 P24_STEP_ACT24 = 0x1
 P24_STEP_KEEP_MASKS = 0x2
 P24_STEP_ADAPTERS = 0x4
@@ -77,6 +78,7 @@ def _load() -> C.CDLL:
         "ffn24_step_traced": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp, C.POINTER(vp), i32]),
         "p24_launch_count": (C.c_uint64, []),
         "p24_query_status": (i32, [vp]),
+        "p24_query_timeout": (i32, [vp, C.POINTER(i64), C.POINTER(i64)]),
         "p24_selftest_timeout": (i32, [i64, vp]),
         "p24_strerror": (C.c_char_p, [i32]),
     }
@@ -197,13 +199,17 @@ def prune24_compress_both(W: torch.Tensor, fwd: Sparse24 | None = None, bwdT: Sp
 
 
 def spmm24_fwd(X: torch.Tensor, W: Sparse24, bias: torch.Tensor | None = None, relu: bool = False,
-               act24: bool = False, Y: torch.Tensor | None = None, Y24: Sparse24 | None = None, stream=None):
-    """Y = act(X W^T + bias); with act24 also returns the 2:4-compressed Y (Y, Y24)."""
+               act24: bool = False, Y: torch.Tensor | None = None, Y24: Sparse24 | None = None, stream=None,
+               test_stall: bool = False):
+    """Y = act(X W^T + bias); with act24 also returns the 2:4-compressed Y (Y, Y24).
+    test_stall (test only): make the kernel's bounded waits expire (P24_EPI_TEST_STALL)."""
     M, K, ldx = _mat(X, name="X")
     N = W.rows
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
     _, _, ldy = _mat(Y, name="Y")
     flags = (P24_EPI_BIAS if bias is not None else 0) | (P24_EPI_RELU if relu else 0)
+    if test_stall:
+        flags |= P24_EPI_TEST_STALL
     y24c = None
     if act24:
         flags |= P24_EPI_ACT24
@@ -449,6 +455,14 @@ def p24_launch_count() -> int:
 def p24_selftest_timeout(limit_ns: int = 10_000_000, stream=None) -> None:
     """Launch the bounded-wait failure self test (see include/prune24.h)."""
     _check(lib.p24_selftest_timeout(limit_ns, _stream(stream)), "p24_selftest_timeout")
+
+
+def p24_query_timeout(stream=None) -> tuple[int, int, int]:
+    """(status, CTA, barrier shared address) of the first expired wait since the last
+    query (-1, -1 when none); clears the status."""
+    cta, bar = C.c_int64(-1), C.c_int64(-1)
+    code = int(lib.p24_query_timeout(_stream(stream), C.byref(cta), C.byref(bar)))
+    return code, cta.value, bar.value
 
 
 def p24_query_status(stream=None) -> int:

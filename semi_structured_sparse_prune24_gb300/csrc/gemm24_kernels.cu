@@ -66,6 +66,7 @@ struct SpmmParams {
   int* status;
   int b3d;  // B map is 3-D: {64 K, rows, K / 64}; one load brings both 64-K halves of a stage
   int nad;  // dense stages per tile after the sparse ones: A_l [rowsA, r] . B_l [rowsB, r]^T, 64 of r each
+  int stall_stage;  // test only: if > 0, both CTAs of cluster 0 skip the loads of their stage number stall_stage - 1
 };
 
 struct DwParams {
@@ -331,6 +332,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         for (int kb = 0; kb < nstages; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          if (p.stall_stage > 0 && cid == 0 && it + 1 == static_cast<uint32_t>(p.stall_stage)) {
+            // test only: no expect_tx and no loads for this stage in either CTA of the
+            // pair, so its `full` barrier never completes and the bounded waits expire
+            if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+            continue;
+          }
           if (kb >= p.nkb) {  // dense stage: 64 of the rank of A_l [rowsA, r] and B_l [rowsB, r]
             if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
             if (leader) mbar_arrive_expect_tx(&full[s], L::kTxDense);
@@ -1009,6 +1016,7 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
   p.gate = static_cast<const uint16_t*>(epi.gate);
   p.ldg = epi.ldg;
   p.dbias = epi.dbias;
+  p.stall_stage = epi.test_stall ? 3 : 0;
   if (!transposed_out && (epi.gate || epi.dbias)) return cudaErrorInvalidValue;
   p.a24_vals = static_cast<uint16_t*>(epi.act24.vals);
   p.a24_ldv = epi.act24.ldv;

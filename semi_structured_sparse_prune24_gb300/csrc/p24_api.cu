@@ -13,7 +13,9 @@
 namespace p24 {
 namespace {
 
-__device__ int g_status;  // P24_OK, or P24_ETIMEOUT after a bounded wait expired
+// [0] P24_OK, or P24_ETIMEOUT after a bounded wait expired; [1] the CTA and [2] the
+// barrier's shared address of the first expired wait; [3] unused
+__device__ int g_status[4];
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
@@ -181,7 +183,8 @@ int check_lowrank(const void* a, int64_t rows_a, int64_t lda, const void* b, int
 
 int fwd_impl(const void* X, int64_t M, int64_t ldx, const p24_sparse* W, const float* bias, uint32_t flags, void* Y,
              int64_t ldy, const p24_sparse* Y24, EpiArgs epi, void* stream) {
-  if (flags & ~(P24_EPI_BIAS | P24_EPI_RELU | P24_EPI_ACT24)) return P24_EINVAL;
+  if (flags & ~(P24_EPI_BIAS | P24_EPI_RELU | P24_EPI_ACT24 | P24_EPI_TEST_STALL)) return P24_EINVAL;
+  epi.test_stall = (flags & P24_EPI_TEST_STALL) != 0;
   P24_TRY(check_sparse(W));
   const int64_t N = W->rows, K = W->cols;
   if (K % 8 != 0 || N % 8 != 0) return P24_EINVAL;
@@ -572,14 +575,18 @@ int p24_selftest_timeout(int64_t limit_ns, void* stream) {
   return cuda_status(launch_selftest_timeout(static_cast<uint64_t>(limit_ns), st, as_stream(stream)));
 }
 
-int p24_query_status(void* stream) {
+int p24_query_timeout(void* stream, int64_t* cta, int64_t* barrier) {
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return P24_ECUDA;
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return P24_ECUDA;
-  const int zero = 0;
-  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return P24_ECUDA;
-  return v;
+  int v[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(v, g_status, sizeof(v)) != cudaSuccess) return P24_ECUDA;
+  const int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) return P24_ECUDA;
+  if (cta) *cta = v[0] ? static_cast<int64_t>(v[1]) : int64_t(-1);
+  if (barrier) *barrier = v[0] ? static_cast<int64_t>(static_cast<uint32_t>(v[2])) : int64_t(-1);
+  return v[0];
 }
+
+int p24_query_status(void* stream) { return p24_query_timeout(stream, nullptr, nullptr); }
 
 const char* p24_strerror(int code) {
   switch (code) {

@@ -36,6 +36,7 @@ struct EpiArgs {
   const void* lr_b = nullptr;
   int64_t lr_ldb = 0;
   int64_t lr_r = 0;
+  bool test_stall = false;  // test only: the first CTA pair skips one stage's loads (its waits expire)
   p24_sparse act24{};           // compressed activation output (vals != null => enabled)
 };
 

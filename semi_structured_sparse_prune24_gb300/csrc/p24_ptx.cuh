@@ -55,6 +55,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with parity `parity` to complete.
 // abort: CTA-shared flag; status: device status word.
+// Status block (int[4]): [0] P24_OK or P24_ETIMEOUT; for the first expired wait,
+// [1] the CTA (blockIdx.x) and [2] the waited-on barrier's shared-memory address.
+__device__ __forceinline__ void p24_record_timeout(int* status, const uint64_t* bar) {
+  if (atomicCAS(status, 0, -4 /* P24_ETIMEOUT */) == 0) {
+    status[1] = static_cast<int>(blockIdx.x);
+    status[2] = static_cast<int>(smem_u32(bar));
+  }
+}
+
 __device__ __forceinline__ bool p24_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                          int* status) {
   const uint32_t a = smem_u32(bar);
@@ -66,7 +75,7 @@ __device__ __forceinline__ bool p24_wait(uint64_t* bar, uint32_t parity, volatil
       if (*abort) return false;
       if (global_ns() - t0 > P24_WAIT_NS) {
         *abort = 1;
-        atomicExch(status, -4 /* P24_ETIMEOUT */);
+        p24_record_timeout(status, bar);
         return false;
       }
     }
@@ -80,7 +89,7 @@ __device__ __forceinline__ bool p24_wait_for(uint64_t* bar, uint32_t parity, uin
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) {
-      atomicExch(status, -4 /* P24_ETIMEOUT */);
+      p24_record_timeout(status, bar);
       return false;
     }
   }

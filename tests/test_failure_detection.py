@@ -31,3 +31,34 @@ def test_selftest_rejects_bad_limits():
     assert N.lib.p24_selftest_timeout(0, None) == N.P24_EINVAL
     assert N.lib.p24_selftest_timeout(-5, None) == N.P24_EINVAL
     assert N.lib.p24_selftest_timeout(10 ** 11, None) == N.P24_EINVAL
+
+
+@pytest.mark.gpu
+def test_sparse_gemm_wait_expires_cleanly_and_reports_where():
+    """The real sparse GEMM with one pipeline stage's loads withheld in its first CTA
+    pair (test-only flag): that pair's bounded waits expire, it drains and exits; the
+    status names the CTA and the barrier; the next call on the same buffers is correct."""
+    import numpy as np
+    import semi_structured_sparse_prune24_gb300 as P
+    from oracle import prune24_oracle as O
+    from synth24 import normal_bf16
+    from tests.conftest import bits_of
+    from tests.p24_testutil import assert_close
+    W = normal_bf16((512, 1024), 0.02, 3, 2, "cuda")
+    X = normal_bf16((512, 1024), 1.0, 3, 1, "cuda")
+    Ws = P.prune24_compress(W)
+    assert P.p24_query_status() == 0
+    Y = P.spmm24_fwd(X, Ws, test_stall=True)
+    code, cta, bar = P.p24_query_timeout()
+    assert code == P24_ETIMEOUT
+    assert cta in (0, 1)                      # a CTA of the first pair
+    # the barrier's shared address as its CTA saw it: the offset in the low 24 bits
+    # (a cluster CTA's window carries its rank above them), within the 227 KB window
+    assert bar >= 0 and (bar & 0xFFFFFF) < 232448
+    assert P.p24_query_timeout() == (0, -1, -1)
+    Y = P.spmm24_fwd(X, Ws, Y=Y)
+    torch.cuda.synchronize()
+    vals, meta = O.compress24(bits_of(W), Ws.ldv, Ws.ldm)
+    ref, _ = O.spmm24_fwd(bits_of(X), vals, meta, 1024)
+    assert_close(Y, ref, "Y after the stalled call")
+    assert P.p24_query_status() == 0
