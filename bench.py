@@ -262,7 +262,7 @@ def run_ours(args, world, rank, local):
                                          "per_launch": gemm_flop, "unit": "TFLOP/s"},
         "dw_kernel (tcgen05.mma, masked)": {"phases": [6, 8], "bound": "tensor", "peak": dense_peak,
                                             "per_launch": gemm_flop, "unit": "TFLOP/s"},
-        "double_prune_kernel (fused prune + double prune)": {
+        "double_prune_interior_kernel (fused prune + double prune)": {
             "phases": [0, 1], "bound": "hbm", "peak": peaks["hbm_gbs"],
             "per_launch": int(4.25 * w.d * w.ffn), "unit": "GB/s"},
         # db_up is fused into the dH GEMM's epilogue; phase 5 is the column sums of dY

@@ -38,6 +38,36 @@ __device__ __forceinline__ uint32_t pick2_nibble(uint32_t lo, uint32_t hi) {
   return min(i_top, i_sec) | (max(i_top, i_sec) << 2);
 }
 
+// The same network, returning which two positions won as a 4-bit code
+// (3 - i_top) << 2 | (3 - i_sec): the row of a 16-entry table (pick_row) that holds
+// everything the caller derives from the decision.
+__device__ __forceinline__ uint32_t pick2_code(uint32_t lo, uint32_t hi) {
+  const uint32_t c0 = ((lo & 0x7FFFu) << 2) | 3u;
+  const uint32_t c1 = ((lo >> 14) & 0x1FFFCu) | 2u;
+  const uint32_t c2 = ((hi & 0x7FFFu) << 2) | 1u;
+  const uint32_t c3 = (hi >> 14) & 0x1FFFCu;
+  const uint32_t a = max(c0, c1), b = min(c0, c1);
+  const uint32_t c = max(c2, c3), d = min(c2, c3);
+  const uint32_t top = max(a, c);
+  const uint32_t second = max(min(a, c), max(b, d));
+  return ((top & 3u) << 2) | (second & 3u);
+}
+
+// Row of the pick table for code t (unused codes, where both positions agree, are 0):
+//   x = byte selector of the kept pair from (lo, hi) | nibble << 16
+//   y = selector keeping lo's kept halves (others from a zero word) | the same for hi << 16
+// A prmt reads only the low 16 bits of its selector.
+__device__ __forceinline__ uint2 pick_row(uint32_t t) {
+  const uint32_t it = 3u - (t >> 2), is = 3u - (t & 3u);
+  if (it == is) return make_uint2(0u, 0u);
+  const uint32_t i0 = min(it, is), i1 = max(it, is);
+  const uint32_t kb = (1u << i0) | (1u << i1);
+  const uint32_t sel_kept = 0x1010u + i0 * 0x22u + i1 * 0x2200u;
+  const uint32_t mlo = ((kb & 1u) ? 0x0010u : 0x0044u) | ((kb & 2u) ? 0x3200u : 0x4400u);
+  const uint32_t mhi = ((kb & 4u) ? 0x0010u : 0x0044u) | ((kb & 8u) ? 0x3200u : 0x4400u);
+  return make_uint2(sel_kept | ((i0 | (i1 << 2)) << 16), mlo | (mhi << 16));
+}
+
 // The two kept values (ascending index) packed as v0 | v1 << 16.
 __device__ __forceinline__ uint32_t kept_pair(uint32_t lo, uint32_t hi, uint32_t nib) {
   const uint32_t i0 = nib & 3u, i1 = nib >> 2;
@@ -122,6 +152,137 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
 }
 
 // ---------------------------------------------------------------- double prune
+constexpr int kDpRows = 128, kDpCols = 128, kDpChunks = kDpCols / 8;
+
+struct DpArgs {
+  const uint16_t* W;        // dense input (kFromDense)
+  int64_t ldw;
+  const uint16_t* fv_in;    // forward values / metadata: read (compressed input) or written
+  uint16_t* fv_out;
+  int64_t ldfv;
+  const uint8_t* fm_in;
+  uint8_t* fm_out;
+  int64_t ldfm;
+  int64_t rows, cols;
+  uint16_t* tv;             // W_bwd^T values / metadata
+  int64_t ldtv;
+  uint8_t* tm;
+  int64_t ldtm;
+  uint16_t* Wm;             // optional dense forward-masked copy
+  int64_t ldwm;
+};
+
+// One 128 x 128 tile. kEdge: the tile crosses the last row or column, so every
+// access is checked; interior tiles (all but a thin border) skip the checks.
+template <bool kFromDense, bool kMasked, bool kEdge>
+__device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t col0, uint4* tile,
+                                        const uint2* ptab) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = threadIdx.x & (kDpChunks - 1);  // load phase: chunk of the thread
+  const int rb = threadIdx.x >> 4;               // load phase: first row of the thread
+  const int64_t e = col0 + 8 * c;
+  const int64_t r_first = row0 + rb;
+
+  // ---------------- load (+ forward prune)
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t row = r_first + 16 * i;
+    v[i] = make_uint4(0, 0, 0, 0);
+    const bool full = !kEdge || (row < p.rows && e + 8 <= p.cols);
+    const bool half = kEdge && row < p.rows && !full && e + 4 <= p.cols;
+    if (kFromDense) {
+      if (full) v[i] = ld_stream_v4(p.W + row * p.ldw + e);
+      else if (half) {
+        const uint2 x = __ldcs(reinterpret_cast<const uint2*>(p.W + row * p.ldw + e));
+        v[i].x = x.x;
+        v[i].y = x.y;
+      }
+    } else if (full || half) {
+      const uint32_t mb = p.fm_in[row * p.ldfm + e / 8];
+      if (full) {
+        const uint2 pr = *reinterpret_cast<const uint2*>(p.fv_in + row * p.ldfv + e / 2);
+        expand_group(pr.x, mb & 0xFu, v[i].x, v[i].y);
+        expand_group(pr.y, mb >> 4, v[i].z, v[i].w);
+      } else {
+        const uint32_t pr = *reinterpret_cast<const uint32_t*>(p.fv_in + row * p.ldfv + e / 2);
+        expand_group(pr, mb & 0xFu, v[i].x, v[i].y);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = rb + 16 * i;
+    const int64_t row = row0 + r;
+    if (kFromDense) {
+      const bool full = !kEdge || (row < p.rows && e + 8 <= p.cols);
+      const bool half = kEdge && row < p.rows && !full && e + 4 <= p.cols;
+      if (full || half) {
+        const uint2 r0 = ptab[pick2_code(v[i].x, v[i].y)];
+        const uint32_t n0 = r0.x >> 16;
+        const uint32_t k0 = __byte_perm(v[i].x, v[i].y, r0.x);
+        v[i].x = __byte_perm(v[i].x, 0u, r0.y);
+        v[i].y = __byte_perm(v[i].y, 0u, r0.y >> 16);
+        if (full) {
+          const uint2 r1 = ptab[pick2_code(v[i].z, v[i].w)];
+          const uint32_t n1 = r1.x >> 16;
+          const uint32_t k1 = __byte_perm(v[i].z, v[i].w, r1.x);
+          v[i].z = __byte_perm(v[i].z, 0u, r1.y);
+          v[i].w = __byte_perm(v[i].w, 0u, r1.y >> 16);
+          *reinterpret_cast<uint2*>(p.fv_out + row * p.ldfv + e / 2) = make_uint2(k0, k1);
+          p.fm_out[row * p.ldfm + e / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
+          if (kMasked) *reinterpret_cast<uint4*>(p.Wm + row * p.ldwm + e) = v[i];
+        } else {
+          *reinterpret_cast<uint32_t*>(p.fv_out + row * p.ldfv + e / 2) = k0;
+          p.fm_out[row * p.ldfm + e / 8] = static_cast<uint8_t>(n0 | 0x40u);
+          if (kMasked) *reinterpret_cast<uint2*>(p.Wm + row * p.ldwm + e) = make_uint2(v[i].x, v[i].y);
+        }
+      }
+    }
+    tile[r * kDpChunks + (c ^ ((r >> 2) & (kDpChunks - 1)))] = v[i];
+  }
+  __syncthreads();
+
+  // ---------------- column groups: lane = row quad, warp = 2 chunks (16 columns)
+  const int h = lane;
+  const int64_t nquads = p.rows / 4;
+  const int64_t hq = row0 / 4 + h;  // global quad = group index along W_bwd^T rows
+  const bool active = !kEdge || hq < nquads;
+  // the quad after an even lane's is inside the matrix unless the tile crosses its end
+  const bool next_in = !kEdge || hq + 1 < nquads;
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int chunk = 2 * warp + cc;
+    const int64_t cbase = col0 + 8 * chunk;
+    if (kEdge && cbase >= p.cols) break;  // uniform per warp
+    uint4 q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = tile[(4 * h + i) * kDpChunks + (chunk ^ (h & (kDpChunks - 1)))];
+    const uint32_t w0[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+    const uint32_t w1[4] = {q[1].x, q[1].y, q[1].z, q[1].w};
+    const uint32_t w2[4] = {q[2].x, q[2].y, q[2].z, q[2].w};
+    const uint32_t w3[4] = {q[3].x, q[3].y, q[3].z, q[3].w};
+    uint16_t* tvp = p.tv + cbase * p.ldtv + 2 * hq;
+    uint8_t* tmp = p.tm + cbase * p.ldtm + hq / 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (kEdge && cbase + j >= p.cols) break;  // uniform per warp
+      const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+      const uint32_t lo = __byte_perm(w0[j >> 1], w1[j >> 1], sel);
+      const uint32_t hi = __byte_perm(w2[j >> 1], w3[j >> 1], sel);
+      const uint32_t row = ptab[pick2_code(lo, hi)].x;
+      const uint32_t nib = row >> 16;
+      const uint32_t pair = __byte_perm(lo, hi, row);
+      const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
+      if (active) {
+        *reinterpret_cast<uint32_t*>(tvp + j * p.ldtv) = pair;
+        if ((lane & 1) == 0) tmp[j * p.ldtm] = static_cast<uint8_t>(nib | ((next_in ? nib_next : 0x4u) << 4));
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // A CTA owns a 128-row x 128-column tile of W_fwd. Load phase: coalesced 16-byte
 // pieces (thread = row piece), the forward prune of dense input happens here and
 // the forward outputs are written straight out; the forward-masked tile goes to
@@ -129,120 +290,57 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
 // the column phase a warp (lane = row quad) reads 4 rows x 16 bytes per lane
 // without bank conflicts. Column phase: each lane prunes the 4-row column groups
 // of its quad and lanes write consecutive groups of a W_bwd^T row (coalesced).
+// Each 2:4 decision indexes a 16-row table (pick_row) in shared memory that holds
+// the kept pair's byte selector, the masking selectors and the nibble.
 // kFromDense: input is the dense W; otherwise the compressed forward matrix.
-constexpr int kDpRows = 128, kDpCols = 128, kDpChunks = kDpCols / 8;
+//
+// Interior tiles (whole 128 x 128 blocks) run without bounds checks, three CTAs
+// per SM; the border tiles of a ragged matrix (the last partial block column, then
+// the last partial block row) run checked in a second, small launch.
+template <bool kFromDense, bool kMasked>
+__global__ void __launch_bounds__(256, 3) double_prune_interior_kernel(const DpArgs p, int64_t rows_full) {
+  __shared__ uint4 tile[kDpRows * kDpChunks];
+  __shared__ uint2 ptab[16];
+  if (threadIdx.x < 16) ptab[threadIdx.x] = pick_row(threadIdx.x);
+  __syncthreads();
+  const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kDpCols;
+  for (int64_t row0 = static_cast<int64_t>(blockIdx.y) * kDpRows; row0 < rows_full;
+       row0 += static_cast<int64_t>(gridDim.y) * kDpRows)
+    dp_tile<kFromDense, kMasked, false>(p, row0, col0, tile, ptab);
+}
 
 template <bool kFromDense, bool kMasked>
-__global__ void __launch_bounds__(256, 2) double_prune_kernel(
-    const uint16_t* __restrict__ W, int64_t ldw,                        // dense input (kFromDense)
-    const uint16_t* __restrict__ fv_in, uint16_t* __restrict__ fv_out,  // forward vals (in / out)
-    int64_t ldfv,
-    const uint8_t* __restrict__ fm_in, uint8_t* __restrict__ fm_out,    // forward meta (in / out)
-    int64_t ldfm, int64_t rows, int64_t cols,
-    uint16_t* __restrict__ tv, int64_t ldtv, uint8_t* __restrict__ tm, int64_t ldtm,
-    uint16_t* __restrict__ Wm, int64_t ldwm) {
+__global__ void __launch_bounds__(256, 2) double_prune_border_kernel(const DpArgs p, int64_t n_col_part,
+                                                                    int64_t full_bx, int64_t full_by) {
   __shared__ uint4 tile[kDpRows * kDpChunks];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kDpCols;
-  const int64_t nquads = rows / 4;
-  const int c = threadIdx.x & (kDpChunks - 1);  // load phase: chunk of the thread
-  const int rb = threadIdx.x >> 4;               // load phase: first row of the thread
+  __shared__ uint2 ptab[16];
+  if (threadIdx.x < 16) ptab[threadIdx.x] = pick_row(threadIdx.x);
+  __syncthreads();
+  const int64_t t = blockIdx.x;
+  const int64_t bx = t < n_col_part ? full_bx : t - n_col_part;
+  const int64_t by = t < n_col_part ? t : full_by;
+  dp_tile<kFromDense, kMasked, true>(p, by * kDpRows, bx * kDpCols, tile, ptab);
+}
 
-  for (int64_t row0 = static_cast<int64_t>(blockIdx.y) * kDpRows; row0 < rows;
-       row0 += static_cast<int64_t>(gridDim.y) * kDpRows) {
-    // ---------------- load (+ forward prune)
-    uint4 v[8];
-    const int64_t e = col0 + 8 * c;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t row = row0 + rb + 16 * i;
-      v[i] = make_uint4(0, 0, 0, 0);
-      const bool full = row < rows && e + 8 <= cols;
-      const bool half = row < rows && !full && e + 4 <= cols;
-      if (kFromDense) {
-        if (full) v[i] = ld_stream_v4(W + row * ldw + e);
-        else if (half) {
-          const uint2 x = __ldcs(reinterpret_cast<const uint2*>(W + row * ldw + e));
-          v[i].x = x.x;
-          v[i].y = x.y;
-        }
-      } else if (full || half) {
-        const uint32_t mb = fm_in[row * ldfm + e / 8];
-        if (full) {
-          const uint2 pr = *reinterpret_cast<const uint2*>(fv_in + row * ldfv + e / 2);
-          expand_group(pr.x, mb & 0xFu, v[i].x, v[i].y);
-          expand_group(pr.y, mb >> 4, v[i].z, v[i].w);
-        } else {
-          const uint32_t pr = *reinterpret_cast<const uint32_t*>(fv_in + row * ldfv + e / 2);
-          expand_group(pr, mb & 0xFu, v[i].x, v[i].y);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = rb + 16 * i;
-      const int64_t row = row0 + r;
-      if (kFromDense) {
-        const bool full = row < rows && e + 8 <= cols;
-        const bool half = row < rows && !full && e + 4 <= cols;
-        if (full || half) {
-          const uint32_t n0 = pick2_nibble(v[i].x, v[i].y);
-          const uint32_t k0 = kept_pair(v[i].x, v[i].y, n0);
-          masked_group(v[i].x, v[i].y, n0, v[i].x, v[i].y);
-          if (full) {
-            const uint32_t n1 = pick2_nibble(v[i].z, v[i].w);
-            const uint32_t k1 = kept_pair(v[i].z, v[i].w, n1);
-            masked_group(v[i].z, v[i].w, n1, v[i].z, v[i].w);
-            *reinterpret_cast<uint2*>(fv_out + row * ldfv + e / 2) = make_uint2(k0, k1);
-            fm_out[row * ldfm + e / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
-            if (kMasked) *reinterpret_cast<uint4*>(Wm + row * ldwm + e) = v[i];
-          } else {
-            *reinterpret_cast<uint32_t*>(fv_out + row * ldfv + e / 2) = k0;
-            fm_out[row * ldfm + e / 8] = static_cast<uint8_t>(n0 | 0x40u);
-            if (kMasked) *reinterpret_cast<uint2*>(Wm + row * ldwm + e) = make_uint2(v[i].x, v[i].y);
-          }
-        }
-      }
-      tile[r * kDpChunks + (c ^ ((r >> 2) & (kDpChunks - 1)))] = v[i];
-    }
-    __syncthreads();
+inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n < 1 ? 1 : n) : 65535); }
 
-    // ---------------- column groups: lane = row quad, warp = 2 chunks (16 columns)
-    const int h = lane;
-    const int64_t hq = row0 / 4 + h;  // global quad = group index along W_bwd^T rows
-    const bool active = hq < nquads;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int chunk = 2 * warp + cc;
-      if (col0 + 8 * chunk >= cols) break;  // uniform per warp
-      uint4 q[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = tile[(4 * h + i) * kDpChunks + (chunk ^ (h & (kDpChunks - 1)))];
-      const uint32_t w0[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
-      const uint32_t w1[4] = {q[1].x, q[1].y, q[1].z, q[1].w};
-      const uint32_t w2[4] = {q[2].x, q[2].y, q[2].z, q[2].w};
-      const uint32_t w3[4] = {q[3].x, q[3].y, q[3].z, q[3].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t col = col0 + 8 * chunk + j;
-        if (col >= cols) break;  // uniform per warp
-        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-        const uint32_t lo = __byte_perm(w0[j >> 1], w1[j >> 1], sel);
-        const uint32_t hi = __byte_perm(w2[j >> 1], w3[j >> 1], sel);
-        const uint32_t nib = pick2_nibble(lo, hi);
-        const uint32_t pair = kept_pair(lo, hi, nib);
-        const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
-        if (active) {
-          *reinterpret_cast<uint32_t*>(tv + col * ldtv + 2 * hq) = pair;
-          if ((lane & 1) == 0) {
-            const uint32_t hi_nib = (hq + 1 < nquads) ? nib_next : 0x4u;
-            tm[col * ldtm + hq / 2] = static_cast<uint8_t>(nib | (hi_nib << 4));
-          }
-        }
-      }
-    }
-    __syncthreads();
+template <bool kFromDense, bool kMasked>
+cudaError_t launch_double_prune(const DpArgs& a, cudaStream_t s) {
+  const int64_t full_bx = a.cols / kDpCols, full_by = a.rows / kDpRows;
+  const int64_t nby = (a.rows + kDpRows - 1) / kDpRows;
+  if (full_bx > 0 && full_by > 0) {
+    dim3 grid(static_cast<unsigned>(full_bx), grid_y(full_by));
+    double_prune_interior_kernel<kFromDense, kMasked><<<grid, 256, 0, s>>>(a, full_by * kDpRows);
+    count_launch();
   }
+  const int64_t n_col_part = (a.cols % kDpCols) ? nby : 0;       // last block column, every block row
+  const int64_t n_row_part = (a.rows % kDpRows) ? full_bx : 0;   // last block row, full block columns
+  if (n_col_part + n_row_part > 0) {
+    double_prune_border_kernel<kFromDense, kMasked>
+        <<<static_cast<unsigned>(n_col_part + n_row_part), 256, 0, s>>>(a, n_col_part, full_bx, full_by);
+    count_launch();
+  }
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- padding
@@ -312,8 +410,6 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns, int* status) {
   fence_barrier_init();
   p24_wait_for(&bar, 0, limit_ns, status);
 }
-
-inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n < 1 ? 1 : n) : 65535); }
 
 }  // namespace
 
@@ -385,18 +481,11 @@ cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t l
 cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& fwd,
                                  const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>((cols + kDpCols - 1) / kDpCols), grid_y((rows + kDpRows - 1) / kDpRows));
   const auto* w = static_cast<const uint16_t*>(W);
-  if (W_masked)
-    double_prune_kernel<true, true><<<grid, 256, 0, s>>>(
-        w, ldw, nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm, rows, cols,
-        static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, static_cast<uint16_t*>(W_masked), ldwm);
-  else
-    double_prune_kernel<true, false><<<grid, 256, 0, s>>>(
-        w, ldw, nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm, rows, cols,
-        static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
+  const DpArgs a{w,       ldw,  nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm,
+                 rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm,
+                 static_cast<uint16_t*>(W_masked), ldwm};
+  cudaError_t e = W_masked ? launch_double_prune<true, true>(a, s) : launch_double_prune<true, false>(a, s);
   if (e != cudaSuccess) return e;
   if ((e = launch_pad(fwd, s)) != cudaSuccess) return e;
   return launch_pad(bwdT, s);
@@ -405,12 +494,9 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
 cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s) {
   const int64_t rows = fwd.rows, cols = fwd.cols;
   if (rows == 0 || cols == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>((cols + kDpCols - 1) / kDpCols), grid_y((rows + kDpRows - 1) / kDpRows));
-  double_prune_kernel<false, false><<<grid, 256, 0, s>>>(
-      nullptr, 0, static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm, rows, cols,
-      static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
+  const DpArgs a{nullptr, 0,    static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm,
+                 rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0};
+  const cudaError_t e = launch_double_prune<false, false>(a, s);
   if (e != cudaSuccess) return e;
   return launch_pad(bwdT, s);
 }
