@@ -294,11 +294,11 @@ __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t c
 // the kept pair's byte selector, the masking selectors and the nibble.
 // kFromDense: input is the dense W; otherwise the compressed forward matrix.
 //
-// Interior tiles (whole 128 x 128 blocks) run without bounds checks, three CTAs
+// Interior tiles (whole 128 x 128 blocks) run without bounds checks, four CTAs
 // per SM; the border tiles of a ragged matrix (the last partial block column, then
 // the last partial block row) run checked in a second, small launch.
 template <bool kFromDense, bool kMasked>
-__global__ void __launch_bounds__(256, 3) double_prune_interior_kernel(const DpArgs p, int64_t rows_full) {
+__global__ void __launch_bounds__(256, 4) double_prune_interior_kernel(const DpArgs p, int64_t rows_full) {
   __shared__ uint4 tile[kDpRows * kDpChunks];
   __shared__ uint2 ptab[16];
   if (threadIdx.x < 16) ptab[threadIdx.x] = pick_row(threadIdx.x);
