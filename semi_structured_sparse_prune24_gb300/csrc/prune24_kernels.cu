@@ -40,12 +40,15 @@ __device__ __forceinline__ uint32_t pick2_nibble(uint32_t lo, uint32_t hi) {
 
 // The same network, returning which two positions won as a 4-bit code
 // (3 - i_top) << 2 | (3 - i_sec): the row of a 16-entry table (pick_row) that holds
-// everything the caller derives from the decision.
+// everything the caller derives from the decision. Here the composite keys are
+// (magnitude << 17) | (3 - i): multiplying a 16-bit value by 2^17 drops its sign
+// bit and everything above it, so each key is one multiply-add (and a shift for
+// the upper half), which keeps the integer ALU pipe free for the min/max network.
 __device__ __forceinline__ uint32_t pick2_code(uint32_t lo, uint32_t hi) {
-  const uint32_t c0 = ((lo & 0x7FFFu) << 2) | 3u;
-  const uint32_t c1 = ((lo >> 14) & 0x1FFFCu) | 2u;
-  const uint32_t c2 = ((hi & 0x7FFFu) << 2) | 1u;
-  const uint32_t c3 = (hi >> 14) & 0x1FFFCu;
+  const uint32_t c0 = lo * 131072u + 3u;
+  const uint32_t c1 = (lo >> 16) * 131072u + 2u;
+  const uint32_t c2 = hi * 131072u + 1u;
+  const uint32_t c3 = (hi >> 16) * 131072u;
   const uint32_t a = max(c0, c1), b = min(c0, c1);
   const uint32_t c = max(c2, c3), d = min(c2, c3);
   const uint32_t top = max(a, c);
