@@ -365,35 +365,54 @@ __global__ void pad_kernel(uint16_t* __restrict__ vals, int64_t ldv, uint8_t* __
 }
 
 // ---------------------------------------------------------------- column sums
-// Pass 1: slab s of rows, 2 columns per thread, fp32 sums in row order.
-__global__ void __launch_bounds__(256) colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int64_t M,
-                                                             int64_t N, int64_t ldg, int64_t rows_per_slab,
-                                                             float* __restrict__ part) {
-  const int64_t col = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 2;
-  const int64_t s = blockIdx.y;
-  if (col >= N) return;
-  const int64_t r0 = s * rows_per_slab;
-  const int64_t r1 = min(M, r0 + rows_per_slab);
-  float a0 = 0.f, a1 = 0.f;
-  if (col + 1 < N) {
-    for (int64_t r = r0; r < r1; ++r) {
-      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(G + r * ldg + col);
-      a0 += __bfloat162float(v.x);
-      a1 += __bfloat162float(v.y);
-    }
-    part[s * N + col] = a0;
-    part[s * N + col + 1] = a1;
-  } else {
-    for (int64_t r = r0; r < r1; ++r) a0 += __bfloat162float(G[r * ldg + col]);
-    part[s * N + col] = a0;
+// Column sums G [M, N] -> out [N] in a fixed order. Pass 1: slab s of
+// rows_per_slab consecutive rows is summed top to bottom, one thread per 8 columns
+// with 16-byte loads (rows start 16-byte aligned: the boundary checks that), 8 rows
+// of loads in flight; a ragged last piece of fewer than 8 columns is read per value.
+// Pass 2 adds the slab partials of each column in slab order.
+__device__ __forceinline__ void add_bf16x8(float* a, const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[2 * k] += __uint_as_float(w[k] << 16);
+    a[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
   }
 }
 
-// Pass 2: fixed-order sum over slabs.
+__global__ void __launch_bounds__(256) colsum_partial_kernel(const uint16_t* __restrict__ G, int64_t M, int64_t N,
+                                                             int64_t ldg, int64_t rows_per_slab,
+                                                             float* __restrict__ part) {
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
+  if (c0 >= N) return;
+  const int64_t s = blockIdx.y;
+  const int64_t r0 = s * rows_per_slab;
+  const int64_t r1 = min(M, r0 + rows_per_slab);
+  const int nc = static_cast<int>(min(static_cast<int64_t>(8), N - c0));
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint16_t* g = G + r0 * ldg + c0;
+  if (nc == 8) {
+    int64_t r = r0;
+    for (; r + 8 <= r1; r += 8, g += 8 * ldg) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(g + i * ldg));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) add_bf16x8(a, v[i]);
+    }
+    for (; r < r1; ++r, g += ldg) add_bf16x8(a, __ldg(reinterpret_cast<const uint4*>(g)));
+  } else {
+    for (int64_t r = r0; r < r1; ++r, g += ldg)
+      for (int j = 0; j < nc; ++j) a[j] += __uint_as_float(static_cast<uint32_t>(g[j]) << 16);
+  }
+  float* o = part + s * N + c0;
+  for (int j = 0; j < nc; ++j) o[j] = a[j];
+}
+
 __global__ void colsum_final_kernel(const float* __restrict__ part, int64_t S, int64_t N, float* __restrict__ out) {
   const int64_t col = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (col >= N) return;
   float a = 0.f;
+#pragma unroll 8
   for (int64_t s = 0; s < S; ++s) a += part[s * N + col];
   out[col] = a;
 }
@@ -505,7 +524,7 @@ cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwd
 }
 
 int64_t colsum_slabs(int64_t M) {
-  int64_t S = (M + 63) / 64;
+  int64_t S = (M + 127) / 128;
   if (S > 1024) S = 1024;
   if (S < 1) S = 1;
   return S;
@@ -545,8 +564,8 @@ cudaError_t launch_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t l
   if (S * N > kNoAllocColsumScratch) S = kNoAllocColsumScratch / N;
   if (S < 1) return cudaErrorInvalidValue;  // rejected on the host before this point
   const int64_t rps = (M + S - 1) / S;
-  dim3 grid(static_cast<unsigned>((N + 511) / 512), static_cast<unsigned>(S));
-  colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), M, N, ldg, rps, ws);
+  dim3 grid(static_cast<unsigned>((N + 2047) / 2048), static_cast<unsigned>(S));
+  colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(G), M, N, ldg, rps, ws);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -560,8 +579,8 @@ cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, floa
   if (M == 0) return cudaMemsetAsync(out, 0, N * sizeof(float), s);
   const int64_t S = colsum_slabs(M);
   const int64_t rps = (M + S - 1) / S;
-  dim3 grid(static_cast<unsigned>((N + 511) / 512), static_cast<unsigned>(S));
-  colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), M, N, ldg, rps, ws);
+  dim3 grid(static_cast<unsigned>((N + 2047) / 2048), static_cast<unsigned>(S));
+  colsum_partial_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(G), M, N, ldg, rps, ws);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
