@@ -65,7 +65,9 @@ def test_compress_wider_strides_and_strided_input(P):
     assert_bits_equal(gm, rm, "meta")
 
 
-@pytest.mark.parametrize("rows,cols", [(4, 8), (8, 12), (132, 72), (128, 1032), (260, 520)])
+# interior tiles only (256, 384); border row only (260, 256); border column only (128, 1032);
+# both (260, 520); narrower than one tile (4, 8), (8, 12), (132, 72)
+@pytest.mark.parametrize("rows,cols", [(4, 8), (8, 12), (132, 72), (128, 1032), (260, 520), (260, 256), (256, 384)])
 @pytest.mark.parametrize("kind", ["normal", "ints", "specials"])
 def test_double_prune_bit_exact(P, rows, cols, kind):
     W = make_w(rows, cols, kind, seed=3)
