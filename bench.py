@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import datetime
 import json
 import os
 import statistics
@@ -76,7 +77,7 @@ class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, device_index: int):
         ident = str(device_index)
@@ -92,7 +93,9 @@ class ClockSampler:
         except Exception:
             self.p = None
 
-    def stop(self) -> dict | None:
+    def stop(self, window: tuple | None = None) -> dict | None:
+        """window: (start, end) local wall-clock datetimes of the timed region; samples
+        outside it are dropped (all are kept if none can be placed inside it)."""
         if self.p is None:
             return None
         time.sleep(0.25)
@@ -102,24 +105,42 @@ class ClockSampler:
         except Exception:
             self.p.kill()
             out, _ = self.p.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
+        return parse_clock_samples(out, window)
+
+
+def parse_clock_samples(text: str, window: tuple | None = None) -> dict | None:
+    """Median SM clock, max clock and active throttle reasons from nvidia-smi CSV lines
+    of ClockSampler.QUERY. Lines whose timestamp falls outside `window` are left out."""
+    import datetime
+    rows = []
+    for line in text.splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm, mx = float(f[1]), float(f[2])
+        except ValueError:
+            continue
+        ts = None
+        if len(f) >= 10:
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[9], "%Y/%m/%d %H:%M:%S.%f")
             except ValueError:
-                continue
-            for name, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                ts = None
+        rows.append((sm, mx, f[5:9], ts))
+    inside = rows
+    if window is not None:
+        lo, hi = window
+        inside = [r for r in rows if r[3] is not None and lo <= r[3] <= hi]
+    in_window = bool(inside)
+    if not inside:
+        inside = rows
+    if not inside:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = {n for r in inside for n, v in zip(names, r[2]) if v.lower() == "active"}
+    return {"sm_mhz": statistics.median(r[0] for r in inside), "sm_max_mhz": max(r[1] for r in inside),
+            "samples": len(inside), "samples_in_timed_region": in_window, "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -238,14 +259,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(local)
     launches0 = P.p24_launch_count()
+    wall0 = datetime.datetime.now()
     t0.record(stream)
     for i in range(args.steps):
         step(handles[i])
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    wall1 = datetime.datetime.now()
     launches = P.p24_launch_count() - launches0
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop((wall0, wall1))
     if P.p24_query_status() != 0:
         raise RuntimeError("device status word set during the timed steps")
     ms_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
@@ -550,7 +573,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="70b_m16384")

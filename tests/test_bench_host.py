@@ -84,3 +84,39 @@ def test_gpu_arm_without_a_gpu_fails_loudly():
                        capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode != 0
     assert not json_lines(r.stdout)
+
+
+def _load_bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", BENCH)
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    return bench
+
+
+def test_clock_samples_are_taken_from_the_timed_region_only():
+    import datetime
+    bench = _load_bench()
+    line = "0, {sm}, 2070, 1200.5, 0x{act}, Not Active, Not Active, {swt}, {cap}, 2026/12/02 21:48:{sec}"
+    text = "\n".join([
+        line.format(sm=2070, act="0", swt="Not Active", cap="Not Active", sec="09.900"),   # before: idle
+        line.format(sm=1700, act="4", swt="Not Active", cap="Active", sec="10.100"),
+        line.format(sm=1760, act="4", swt="Not Active", cap="Active", sec="10.300"),
+        line.format(sm=1800, act="4", swt="Not Active", cap="Active", sec="10.500"),
+        line.format(sm=1500, act="20", swt="Active", cap="Not Active", sec="11.200"),      # after the region
+        "garbage line",
+    ])
+    lo = datetime.datetime(2026, 12, 2, 21, 48, 10)
+    hi = datetime.datetime(2026, 12, 2, 21, 48, 10, 600000)
+    c = bench.parse_clock_samples(text, (lo, hi))
+    assert c["samples"] == 3 and c["samples_in_timed_region"] is True
+    assert c["sm_mhz"] == 1760 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]                 # the thermal flag after the region is ignored
+    # no sample inside the window (or no parsable timestamps): every sample is kept and flagged so
+    far = (datetime.datetime(2027, 1, 1), datetime.datetime(2027, 1, 2))
+    c = bench.parse_clock_samples(text, far)
+    assert c["samples"] == 5 and c["samples_in_timed_region"] is False
+    assert c["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    old = "\n".join(l.rsplit(",", 1)[0] for l in text.splitlines()[:3])   # lines without the timestamp field
+    c = bench.parse_clock_samples(old, (lo, hi))
+    assert c["samples"] == 3 and c["samples_in_timed_region"] is False
+    assert bench.parse_clock_samples("", None) is None
