@@ -273,9 +273,9 @@ __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t c
       const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
       const uint32_t lo = __byte_perm(w0[j >> 1], w1[j >> 1], sel);
       const uint32_t hi = __byte_perm(w2[j >> 1], w3[j >> 1], sel);
-      const uint32_t row = ptab[pick2_code(lo, hi)].x;
-      const uint32_t nib = row >> 16;
-      const uint32_t pair = __byte_perm(lo, hi, row);
+      const uint32_t entry = ptab[pick2_code(lo, hi)].x;
+      const uint32_t nib = entry >> 16;
+      const uint32_t pair = __byte_perm(lo, hi, entry);
       const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
       if (active) {
         *reinterpret_cast<uint32_t*>(tvp + j * p.ldtv) = pair;
