@@ -114,3 +114,35 @@ def test_workspace_sizes_grow_with_the_problem(native):
     assert f(128, 256, 512, 0) < f(256, 256, 512, 0) < f(256, 256, 512, native.P24_STEP_ACT24)
     assert native.lib.p24_colsum_workspace_size(64, 100) == 400
     assert native.lib.p24_colsum_workspace_size(10 ** 6, 8) == 1024 * 8 * 4
+
+
+def test_host_validation_of_the_fused_lowrank_dense_and_colsum_calls(native):
+    L = native.lib
+    EINVAL, EALIGN, ENOSPACE = native.P24_EINVAL, native.P24_EALIGN, native.P24_ENOSPACE
+    fake = 0x10000  # never dereferenced: every call below fails validation first
+    fwd = _sp(fake, fake, 16, 32, 16, 16, native)      # W [16, 32]
+    bwdT = _sp(fake, fake, 32, 16, 8, 16, native)      # W_bwd^T [32, 16]
+    # fused prune-both: rows and cols multiples of 4, transposed descriptor shapes, aligned masked copy
+    assert L.prune24_compress_both(fake, 14, 32, 32, C.byref(fwd), C.byref(bwdT), None, 0, None) == EINVAL
+    assert L.prune24_compress_both(fake, 16, 30, 32, C.byref(fwd), C.byref(bwdT), None, 0, None) == EINVAL
+    same = _sp(fake, fake, 16, 32, 16, 16, native)
+    assert L.prune24_compress_both(fake, 16, 32, 32, C.byref(fwd), C.byref(same), None, 0, None) == EINVAL
+    assert L.prune24_compress_both(fake, 16, 32, 32, C.byref(fwd), C.byref(bwdT), fake + 2, 32, None) == EALIGN
+    # allocation-free colsum: wider than its fixed scratch
+    wide = (1 << 20) + 8
+    assert L.p24_colsum_noalloc(fake, 4, wide, wide, fake, None) == ENOSPACE
+    # low-rank calls: rank a multiple of 8, 16-byte factor strides, factors present
+    w = _sp(fake, fake, 16, 16, 8, 16, native)
+    assert L.spmm24_fwd_lowrank(fake, 8, 16, C.byref(w), fake, 12, fake, 12, 12, None, 0, fake, 16, None,
+                                None) == EINVAL
+    assert L.spmm24_fwd_lowrank(fake, 8, 16, C.byref(w), fake, 20, fake, 16, 16, None, 0, fake, 16, None,
+                                None) == EALIGN
+    assert L.spmm24_bwd_dx_lowrank(fake, 8, 16, C.byref(w), fake, 16, None, 16, 16, None, 0, fake, 16, None,
+                                   None) == EINVAL
+    # dense rank-r products: K >= 0, strides cover the rows and are multiples of 8 elements
+    assert L.p24_gemm_nt(fake, 8, 16, fake, 8, 16, -1, fake, 8, None) == EINVAL
+    assert L.p24_gemm_nt(fake, 8, 8, fake, 8, 16, 16, fake, 8, None) == EINVAL
+    assert L.p24_gemm_tn(fake, 16, fake, 20, 8, 16, 16, fake, 16, None) == EALIGN
+    # transpose: 2-byte alignment, strides cover the rows
+    assert L.p24_transpose(fake + 1, 4, 4, 4, fake, 4, None) == EALIGN
+    assert L.p24_transpose(fake, 4, 8, 4, fake, 4, None) == EINVAL
