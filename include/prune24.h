@@ -112,6 +112,33 @@ int prune24_transpose_repack(const p24_sparse* fwd, const p24_sparse* bwdT,
                              void* stream);
 
 /*
+ * vnm24_compress -- V:2:M vector-wise N:M pruning (the VENOM format named in
+ * the ESPLAG success story, "Solution"; v:n:m activation sparsity in the TO24
+ * abstract). The pages give no layout, parameters or selection rule; this call
+ * implements the following reading of them.
+ *   - A [rows, cols] bf16 (row stride lda) is pruned along cols.
+ *   - In every block of V consecutive rows (the last block may be shorter) and
+ *     every group of M consecutive columns, the same 4 columns are kept for all
+ *     rows of the block: the 4 with the largest L1 norm over the block (fp32
+ *     sum, rows in order; compared as the sum's bit pattern, every NaN equal
+ *     and above inf; ties to the lower column).
+ *   - Each row then keeps 2 of its values at those 4 columns by the 2:4 rule of
+ *     prune24_compress.
+ *   V >= 1; M in {4, 8, 16, 32, 64, 128}; cols % M == 0. M = 4 is plain 2:4.
+ * Outputs (caller-owned device memory):
+ *   colidx : uint8 [ceil(rows/V), cols/M, 4], the kept column offsets (0..M-1)
+ *            of each block and group, ascending.
+ *   out    : descriptor of the condensed matrix, rows = rows, cols = 4*cols/M:
+ *            row r, group g holds A's values at the 4 kept columns of g in the
+ *            2:4 format of prune24_compress (values, nibbles, padding).
+ * Returns P24_EINVAL for bad V, M, shapes or null pointers, P24_EALIGN for
+ * misaligned A or out; nothing is launched then.
+ */
+int vnm24_compress(const void* A, int64_t rows, int64_t cols, int64_t lda,
+                   int64_t V, int64_t M, uint8_t* colidx, const p24_sparse* out,
+                   void* stream);
+
+/*
  * prune24_compress_both -- prune24_compress followed by
  * prune24_transpose_repack in one pass over the dense W (the per-step mask
  * recompute of gradual magnitude pruning, ESPLAG success story, "Research

@@ -12,11 +12,11 @@ from ._native import (P24_EPI_ACT24, P24_EPI_BIAS, P24_EPI_RELU, P24_STEP_ACT24,
                       lib, masked_dw_gemm, p24_colsum, p24_colsum_noalloc, p24_gemm_nt, p24_gemm_tn,
                       p24_launch_count, p24_query_status, p24_query_timeout, p24_selftest_timeout, p24_transpose, prune24_compress,
                       prune24_compress_both, prune24_transpose_repack, spmm24_bwd_dx, spmm24_bwd_dx_lowrank,
-                      spmm24_fwd, spmm24_fwd_lowrank, spmm24_fwd_sparse_act)
+                      spmm24_fwd, spmm24_fwd_lowrank, spmm24_fwd_sparse_act, vnm24_compress)
 
 __all__ = [
     "P24Error", "Sparse24", "lib", "ld_meta", "ld_vals",
-    "prune24_compress", "prune24_compress_both", "prune24_transpose_repack",
+    "prune24_compress", "prune24_compress_both", "prune24_transpose_repack", "vnm24_compress",
     "spmm24_fwd", "spmm24_fwd_sparse_act", "spmm24_bwd_dx", "masked_dw_gemm",
     "spmm24_fwd_lowrank", "spmm24_bwd_dx_lowrank", "p24_gemm_nt", "p24_gemm_tn", "p24_transpose",
     "p24_colsum", "p24_colsum_noalloc", "ffn24_step", "ffn24_workspace_size", "ffn24_workspace_size_lowrank",

@@ -60,6 +60,7 @@ def _load() -> C.CDLL:
         "prune24_compress": (i32, [vp, i64, i64, i64, sp, vp, i64, vp]),
         "prune24_transpose_repack": (i32, [sp, sp, vp]),
         "prune24_compress_both": (i32, [vp, i64, i64, i64, sp, sp, vp, i64, vp]),
+        "vnm24_compress": (i32, [vp, i64, i64, i64, i64, i64, vp, sp, vp]),
         "spmm24_fwd": (i32, [vp, i64, i64, sp, vp, u32, vp, i64, sp, vp]),
         "spmm24_fwd_sparse_act": (i32, [sp, vp, i64, i64, vp, u32, vp, i64, vp]),
         "spmm24_bwd_dx": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, vp, vp]),
@@ -182,6 +183,23 @@ def prune24_transpose_repack(fwd: Sparse24, bwdT: Sparse24 | None = None, stream
     a, b = fwd.c(), bwdT.c()
     _check(lib.prune24_transpose_repack(C.byref(a), C.byref(b), _stream(stream)), "prune24_transpose_repack")
     return bwdT
+
+
+def vnm24_compress(A: torch.Tensor, V: int, M: int, out: Sparse24 | None = None,
+                   colidx: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, Sparse24]:
+    """V:2:M prune of A along its columns: (colidx uint8 [ceil(rows/V), cols/M, 4],
+    the condensed [rows, 4 cols/M] matrix compressed 2:4)."""
+    rows, cols, lda = _mat(A, name="A")
+    if M <= 0 or cols % M:
+        raise P24Error(P24_EINVAL, f"vnm24_compress: cols={cols} is not a multiple of M={M}")
+    nb = (rows + V - 1) // V if V > 0 else 0
+    out = Sparse24.empty(rows, 4 * (cols // M), A.device) if out is None else out
+    if colidx is None:
+        colidx = torch.empty((nb, cols // M, 4), dtype=torch.uint8, device=A.device)
+    d = out.c()
+    _check(lib.vnm24_compress(A.data_ptr(), rows, cols, lda, V, M, colidx.data_ptr(), C.byref(d), _stream(stream)),
+           "vnm24_compress")
+    return colidx, out
 
 
 def prune24_compress_both(W: torch.Tensor, fwd: Sparse24 | None = None, bwdT: Sparse24 | None = None,

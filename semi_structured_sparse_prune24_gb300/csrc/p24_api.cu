@@ -165,6 +165,19 @@ int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw
   return cuda_status(launch_compress_both(W, rows, cols, ldw, *fwd, *bwdT, W_masked, ldwm, as_stream(stream)));
 }
 
+int vnm24_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int64_t V, int64_t M, uint8_t* colidx,
+                   const p24_sparse* out, void* stream) {
+  if (V < 1 || V > kMaxDim) return P24_EINVAL;
+  if (M < 4 || M > 128 || M % 4 != 0 || 256 % M != 0) return P24_EINVAL;
+  if (cols % M != 0) return P24_EINVAL;
+  P24_TRY(check_dense(A, rows, cols, lda));
+  P24_TRY(check_sparse(out));
+  if (out->rows != rows || out->cols != 4 * (cols / M)) return P24_EINVAL;
+  if (rows > 0 && cols > 0 && !colidx) return P24_EINVAL;
+  return cuda_status(launch_vnm_compress(A, rows, cols, lda, static_cast<int>(V), static_cast<int>(M), colidx, *out,
+                                         as_stream(stream)));
+}
+
 namespace {
 // the rank-r term of a low-rank call: rows of its two factors and their strides
 int check_lowrank(const void* a, int64_t rows_a, int64_t lda, const void* b, int64_t rows_b, int64_t ldb, int64_t r,

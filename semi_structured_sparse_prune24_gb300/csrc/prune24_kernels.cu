@@ -154,6 +154,90 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
   }
 }
 
+// ---------------------------------------------------------------- V:2:M prune
+// Vector-wise N:M (the VENOM format of the ESPLAG success story, "Solution"; v:n:m
+// activations in the TO24 abstract): in every block of V rows and group of M
+// columns the same 4 columns are kept for all rows of the block (the 4 largest
+// L1 norms over the block, ties to the lower column), then each row keeps 2 of
+// those 4 by the 2:4 rule. Output: the selected column offsets, and the condensed
+// [rows, 4 cols / M] matrix in the 2:4 format.
+//
+// A CTA owns one block of rows and 256 consecutive columns (M divides 256, so
+// groups never straddle CTAs, and with M <= 128 a CTA holds whole pairs of groups,
+// i.e. whole metadata bytes).
+//   1. thread = column: its L1 norm over the block, fp32, rows in order; the
+//      ranking key is the sum's bit pattern (every NaN as 0x7FC00000);
+//   2. thread = column: kept iff fewer than 4 columns of its group beat it
+//      (larger key, or equal key and lower column); its rank among the kept
+//      columns of the group gives its slot in the ascending offset list;
+//   3. threads = (row, pair of groups): the 4 values at the kept columns are
+//      pruned 2:4 and written as values plus one metadata byte.
+constexpr int kVnmCols = 256;
+
+__global__ void __launch_bounds__(256) vnm_compress_kernel(const uint16_t* __restrict__ A, int64_t rows,
+                                                           int64_t cols, int64_t lda, int V, int M,
+                                                           uint8_t* __restrict__ colidx, uint16_t* __restrict__ vals,
+                                                           int64_t ldv, uint8_t* __restrict__ meta, int64_t ldm) {
+  __shared__ uint32_t key[kVnmCols];
+  __shared__ uint8_t kept[kVnmCols];
+  __shared__ uint8_t offs[kVnmCols];  // [group in chunk][slot 0..3]: up to 64 groups of 4
+  const int t = threadIdx.x;
+  const int64_t G = cols / M;                    // groups per row
+  const int64_t nb = (rows + V - 1) / V;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kVnmCols;
+  const int64_t c = c0 + t;
+  const int j = t % M, gstart = t - j;           // column within its group, group's first thread
+  const int gpc = kVnmCols / M;                  // groups per chunk (even: M <= 128)
+  for (int64_t b = blockIdx.y; b < nb; b += gridDim.y) {
+    const int64_t r0 = b * V;
+    const int64_t r1 = min(rows, r0 + V);
+    // 1. column norm over the block
+    float sum = 0.f;
+    if (c < cols)
+      for (int64_t r = r0; r < r1; ++r) sum += __uint_as_float(static_cast<uint32_t>(A[r * lda + c] & 0x7FFFu) << 16);
+    const uint32_t k = (sum != sum) ? 0x7FC00000u : __float_as_uint(sum);
+    key[t] = k;
+    __syncthreads();
+    // 2. selection and slot
+    int beat = 0;
+    for (int q = 0; q < M; ++q) {
+      const uint32_t kq = key[gstart + q];
+      beat += (kq > k || (kq == k && q < j)) ? 1 : 0;
+    }
+    kept[t] = beat < 4 ? 1 : 0;
+    __syncthreads();
+    if (kept[t]) {
+      int slot = 0;
+      for (int q = 0; q < j; ++q) slot += kept[gstart + q];
+      offs[(t / M) * 4 + slot] = static_cast<uint8_t>(j);
+      if (c < cols) colidx[(b * G + c / M) * 4 + slot] = static_cast<uint8_t>(j);
+    }
+    __syncthreads();
+    // 3. rows of the block x pairs of groups of the chunk
+    const int pairs = gpc / 2;
+    const int64_t g_first = c0 / M;              // even
+    const int64_t nwork = (r1 - r0) * pairs;
+    for (int64_t w = t; w < nwork; w += blockDim.x) {
+      const int64_t r = r0 + w / pairs;
+      const int pl = static_cast<int>(w % pairs);
+      uint32_t nib[2] = {0x4u, 0x4u};
+      for (int h = 0; h < 2; ++h) {
+        const int gl = 2 * pl + h;               // group within the chunk
+        const int64_t gg = g_first + gl;         // group within the row
+        if (gg >= G) break;
+        const uint16_t* a = A + r * lda + gg * M;
+        const uint8_t* o = offs + gl * 4;
+        const uint32_t lo = static_cast<uint32_t>(a[o[0]]) | (static_cast<uint32_t>(a[o[1]]) << 16);
+        const uint32_t hi = static_cast<uint32_t>(a[o[2]]) | (static_cast<uint32_t>(a[o[3]]) << 16);
+        nib[h] = pick2_nibble(lo, hi);
+        *reinterpret_cast<uint32_t*>(vals + r * ldv + 2 * gg) = kept_pair(lo, hi, nib[h]);
+      }
+      if (g_first + 2 * pl < G) meta[r * ldm + (g_first + 2 * pl) / 2] = static_cast<uint8_t>(nib[0] | (nib[1] << 4));
+    }
+    __syncthreads();
+  }
+}
+
 // ---------------------------------------------------------------- double prune
 constexpr int kDpRows = 128, kDpCols = 128, kDpChunks = kDpCols / 8;
 
@@ -511,6 +595,19 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
   if (e != cudaSuccess) return e;
   if ((e = launch_pad(fwd, s)) != cudaSuccess) return e;
   return launch_pad(bwdT, s);
+}
+
+cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
+                                uint8_t* colidx, const p24_sparse& out, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t nb = (rows + V - 1) / V;
+  dim3 grid(static_cast<unsigned>((cols + kVnmCols - 1) / kVnmCols), grid_y(nb));
+  vnm_compress_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(A), rows, cols, lda, V, M, colidx,
+                                            static_cast<uint16_t*>(out.vals), out.ldv, out.meta, out.ldm);
+  count_launch();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_pad(out, s);
 }
 
 cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s) {

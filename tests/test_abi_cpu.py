@@ -146,3 +146,17 @@ def test_host_validation_of_the_fused_lowrank_dense_and_colsum_calls(native):
     # transpose: 2-byte alignment, strides cover the rows
     assert L.p24_transpose(fake + 1, 4, 4, 4, fake, 4, None) == EALIGN
     assert L.p24_transpose(fake, 4, 8, 4, fake, 4, None) == EINVAL
+
+
+def test_host_validation_of_vnm24_compress(native):
+    L = native.lib
+    EINVAL, EALIGN = native.P24_EINVAL, native.P24_EALIGN
+    fake = 0x10000  # never dereferenced: every call below fails validation first
+    out = _sp(fake, fake, 8, 16, 8, 16, native)          # condensed [8, 4*32/8 = 16]
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 12, fake, C.byref(out), None) == EINVAL   # M not dividing 256
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 256, fake, C.byref(out), None) == EINVAL  # M above 128
+    assert L.vnm24_compress(fake, 8, 36, 40, 4, 8, fake, C.byref(out), None) == EINVAL    # cols % M
+    assert L.vnm24_compress(fake, 8, 32, 32, 0, 8, fake, C.byref(out), None) == EINVAL    # V < 1
+    assert L.vnm24_compress(fake, 8, 32, 36, 4, 8, fake, C.byref(out), None) == EALIGN    # lda % 8
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 16, fake, C.byref(out), None) == EINVAL   # out is not [8, 8]
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 8, None, C.byref(out), None) == EINVAL    # no colidx
