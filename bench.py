@@ -450,6 +450,32 @@ def run_ours(args, world, rank, local):
                  "note": "input 2 GB > L2, no flush needed"}
         del Wp, sp
         torch.cuda.empty_cache()
+        # ---- V:2:M prune (128:2:8, 75% sparse) of a W_up-shaped weight [ffn, d]
+        try:
+            Wv = normal_bf16((w.ffn, w.d), w.w_sigma, seed, 2, dev)
+            ci, vs = P.vnm24_compress(Wv, 128, 8)
+            for _ in range(args.warmup):
+                P.vnm24_compress(Wv, 128, 8, out=vs, colidx=ci)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(args.steps):
+                P.vnm24_compress(Wv, 128, 8, out=vs, colidx=ci)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            vms = e0.elapsed_time(e1) / args.steps
+            # read 2 B; write 2 of every 8 values (0.5 B) and one nibble per 8 (0.0625 B); 4 B per 128 x 8 block
+            per_elt = 2 + 0.5 + 0.0625 + 4 / (128 * 8)
+            vgbs = per_elt * Wv.numel() / (vms * 1e-3) / 1e9
+            prune["vnm_128_2_8"] = {"value": vgbs, "unit": "GB/s", "ms": vms, "frac_hbm": vgbs / peaks["hbm_gbs"],
+                                    "shape": [w.ffn, w.d], "algorithmic_bytes_per_elt": per_elt,
+                                    "note": f"vnm24_compress, input {Wv.numel() * 2 >> 20} MB" +
+                                            (" > L2, no flush needed" if Wv.numel() * 2 > L2_BYTES else
+                                             " (fits in L2: L2-warm)")}
+            del Wv, ci, vs
+        except Exception as exc:  # a failure here must not cost the bench line
+            prune["vnm_128_2_8"] = {"error": f"{type(exc).__name__}: {exc}"}
+        torch.cuda.empty_cache()
         ws = torch.empty(P.ffn24_workspace_size(w.M, w.d, w.ffn, w.act24), dtype=torch.uint8, device=dev)
 
     # ---- end to end through the public API with host buffers
