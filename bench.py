@@ -7,7 +7,8 @@ forward, double-pruned backward, masked weight gradients) on GB300.
 Prints ONE JSON line on rank 0. The metric is the step's dense-equivalent
 throughput (12 * M * d * ffn FLOP per step / step time), reported with its
 fraction of the 2:4-sparse bf16 tensor peak; the standalone 1e9-element prune
-is reported beside it in GB/s. Multi-GPU runs are independent replicas (one
+and the V:2:M (128:2:8) prune of a W_up-shaped weight are reported beside it in
+GB/s. Multi-GPU runs are independent replicas (one
 step per GPU, no collective on the data path): weak scaling, value = all
 ranks' FLOP / the slowest rank's time.
 
