@@ -16,9 +16,6 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
                                  const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s);
 cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s);
 cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s);
-// V:2:M prune + compress: colidx [ceil(rows/V), cols/M, 4]; out = the condensed [rows, 4 cols/M] matrix.
-cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
-                                uint8_t* colidx, const p24_sparse& out, cudaStream_t s);
 int64_t colsum_slabs(int64_t M);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s);
