@@ -11,6 +11,11 @@
 #include "p24_internal.h"
 
 namespace p24 {
+// V:2:M prune + compress (prune24_kernels.cu): colidx [ceil(rows/V), cols/M, 4];
+// out = the condensed [rows, 4 cols/M] matrix in the 2:4 format.
+cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
+                                uint8_t* colidx, const p24_sparse& out, cudaStream_t s);
+
 namespace {
 
 // [0] P24_OK, or P24_ETIMEOUT after a bounded wait expired; [1] the CTA and [2] the
@@ -164,13 +169,6 @@ int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw
   if (W_masked) P24_TRY(check_dense(W_masked, rows, cols, ldwm));
   return cuda_status(launch_compress_both(W, rows, cols, ldw, *fwd, *bwdT, W_masked, ldwm, as_stream(stream)));
 }
-
-namespace p24 {
-// V:2:M prune + compress (prune24_kernels.cu): colidx [ceil(rows/V), cols/M, 4];
-// out = the condensed [rows, 4 cols/M] matrix in the 2:4 format.
-cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
-                                uint8_t* colidx, const p24_sparse& out, cudaStream_t s);
-}  // namespace p24
 
 int vnm24_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int64_t V, int64_t M, uint8_t* colidx,
                    const p24_sparse* out, void* stream) {
