@@ -42,7 +42,7 @@ def test_reference_arm_prints_one_contract_line():
 
 
 def test_reference_arm_under_torchrun_two_ranks():
-    """N=2 as the driver launches it: rank 0 alone runs and prints, rank 1 exits 0."""
+    """N=2 under torch.distributed.run: rank 0 alone runs and prints, rank 1 exits 0."""
     env = dict(os.environ, OMP_NUM_THREADS="2")
     r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
                         "--master-addr", "127.0.0.1", "--master-port", str(free_port()), BENCH,
