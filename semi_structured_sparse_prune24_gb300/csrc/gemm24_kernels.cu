@@ -17,11 +17,13 @@
 // sparse backward); "To 2:4 Sparsity and Beyond" abstract (2:4 weights and
 // sparse activations in all FFN matmuls).
 //
-// Both kernels run as clusters of 2 CTAs (one per SM). The two CTAs of a cluster
-// own adjacent A tiles and share one B tile: each loads half of the B tile and
-// TMA-multicasts it to both, which halves the B traffic from L2. A stage is
-// refilled only after both CTAs' MMAs released it (the MMA commit is multicast
-// to the empty barrier of both CTAs).
+// Both kernels run as CTA pairs (clusters of 2 CTAs, one per SM) issuing
+// cta_group::2 MMAs of M = 256: the two CTAs own adjacent 128-row halves of the A
+// tile and each stages half of the shared B tile, which the tensor cores of the
+// pair read from both CTAs' shared memory, so B crosses L2 once per pair. The
+// leader CTA issues the MMAs; one MMA commit, signalled to both CTAs, frees a
+// stage in both. Every load is a plain (non-multicast) TMA copy into the
+// issuing CTA's own shared memory.
 //
 // Roles (warp index): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 epilogue
 // (warp w reads TMEM lanes 32*(w%4)..+31), 6-9 (spmm only) metadata movers:
@@ -644,19 +646,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
 }
 
-// ---------------------------------------------------------------- masked dW GEMM
-// Per stage (64 tokens): A = dY tile [64 tokens x 128 features] as two 64-wide
-// boxes, B = X tile [64 tokens x 256 columns] as four 64-wide boxes; 128B
-// swizzle, MN-major for both operands.
+// ---------------------------------------------------------------- masked dW GEMM (CTA pair)
+// A cluster of 2 CTAs computes each 256 x 256 tile of dW with pair MMAs
+// (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16). CTA c of the pair holds
+// dW rows 128c..128c+127 of the tile (its A operand: dY's 128 features) and
+// columns 128c..128c+127 of the tile's B operand (X's columns), so each SM stages
+// and reads only half of B; CTA 0 (the leader) issues the MMAs and both CTAs'
+// loads complete on its `full` barrier. Each CTA's TMEM receives the accumulator
+// rows of its own 128 dW rows. Per stage (64 tokens) per CTA: A = dY [64 tokens x
+// 128 features] and B = X [64 tokens x 128 columns], each as two 64-wide boxes
+// (128 B rows, 128B swizzle), MN-major for both operands.
 template <int STAGES>
 struct DwSmem {
   static constexpr int kA = 64 * 128 * 2;
-  static constexpr int kB = 64 * 256 * 2;
+  static constexpr int kB = 64 * 128 * 2;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
-  static constexpr int kOffBar = kOffB + STAGES * kB;
+  // spare bytes after the last B stage: a B descriptor covers this CTA's 128
+  // columns, and the pad keeps even a read of the full 256 inside the allocation
+  static constexpr int kPad = 2 * 8192;
+  static constexpr int kOffBar = kOffB + STAGES * kB + kPad;
   static constexpr int kBytes = kOffBar + 8 * (2 * STAGES + 5) + 16;
-  static constexpr int kTx = kA + kB;
+  static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
 };
 
 template <int STAGES, bool kMasked>
@@ -665,13 +676,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
               const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, const DwParams p) {
   using L = DwSmem<STAGES>;
   constexpr int BN = 256;
-  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false, /*a_mn=*/true, /*b_mn=*/true);
+  constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, false, /*a_mn=*/true, /*b_mn=*/true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
-  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // leader's is used
+  uint64_t* empty = full + STAGES;                                    // leader's commit, both CTAs
+  uint64_t* acc_full = empty + STAGES;                                // [2] leader's commit, both CTAs
+  uint64_t* acc_empty = acc_full + 2;                                 // [2] leader's is used (8 arrivals)
   uint64_t* spare = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -681,11 +692,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // one MMA commit from each CTA of the cluster
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], 8);  // 4 epilogue warps x 2 CTAs
     }
     mbar_init(spare, 1);
     *abort_flag = 0;
@@ -695,18 +706,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (p.tilesA_main < p.tilesA) tma_prefetch_desc(&tmA2);
     if (p.tilesB_main < p.tilesB) tma_prefetch_desc(&tmB2);
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+  if (warp == 1) {  // pair allocation: one warp of each CTA, same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -718,62 +733,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const CUtensorMap* ma = xa ? &tmA2 : &tmA;
         const CUtensorMap* mb = xb ? &tmB2 : &tmB;
         const int a0 = (2 * (xa ? ta - p.tilesA_main : ta) + rank) * kBM;
-        const int b0 = (xb ? tb - p.tilesB_main : tb) * BN;
+        const int b0 = (xb ? tb - p.tilesB_main : tb) * BN + rank * (BN / 2);
         for (int kb = 0; kb < p.nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], L::kTx);
+          if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
+          const uint32_t fullL = leader_addr(&full[s]);
           uint8_t* a = smem + L::kOffA + s * L::kA;
           uint8_t* b = smem + L::kOffB + s * L::kB;
-          for (int i = 0; i < 2; ++i) tma_load_2d(a + i * 8192, ma, &full[s], a0 + i * 64, kb * 64);
-          for (int i = 2 * rank; i < 2 * rank + 2; ++i)
-            tma_load_2d_mc(b + i * 8192, mb, &full[s], b0 + i * 64, kb * 64, 0x3);
+          for (int i = 0; i < 2; ++i) tma_load_2d_pair(a + i * 8192, ma, fullL, a0 + i * 64, kb * 64);
+          for (int i = 0; i < 2; ++i) tma_load_2d_pair(b + i * 8192, mb, fullL, b0 + i * 64, kb * 64);
         }
       }
+      // Drain: the last issued loads must land before the CTA may exit.
       const uint32_t n_drain = it < STAGES ? it : STAGES;
       for (uint32_t i = 0; i < n_drain; ++i) {
         const uint32_t j = it - 1 - i;
-        p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
+        if (leader) p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
       }
     }
   } else if (warp == 1) {
-    uint32_t it = 0, tl = 0;
-    bool ok = true;
-    for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
-      const int b = tl & 1;
-      const uint32_t aph = (tl >> 1) & 1;
-      if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + b * BN;
-      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!p24_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
+    // ------------------------------------------------ MMA issuer (leader CTA only)
+    if (leader) {
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl, ++tl) {
+        const int b = tl & 1;
+        const uint32_t aph = (tl >> 1) & 1;
+        if (!p24_wait(&acc_empty[b], aph ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
-          const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
+        const uint32_t d_tmem = tmem + b * BN;
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!p24_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_base = smem_u32(smem + L::kOffA + s * L::kA);
+            const uint32_t b_base = smem_u32(smem + L::kOffB + s * L::kB);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc(a_base + kk * 2048, 8192, 1024, kSwizzle128B);
-            const uint64_t bdesc = smem_desc(b_base + kk * 2048, 8192, 1024, kSwizzle128B);
-            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t adesc = smem_desc(a_base + kk * 2048, 8192, 1024, kSwizzle128B);
+              const uint64_t bdesc = smem_desc(b_base + kk * 2048, 8192, 1024, kSwizzle128B);
+              tc_mma_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0);
+            }
+            tc_commit_pair(&empty[s], 0x3);
           }
-          tc_commit_mc(&empty[s], 0x3);
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair(&acc_full[b], 0x3);
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&acc_full[b]);
+      // Make sure no MMA is still running before TMEM is released.
+      if (lane == 0) {
+        tc_commit_pair(spare, 0x1);
+        p24_wait_quiet(spare, 0);
+      }
       __syncwarp();
     }
-    if (lane == 0) {
-      tc_commit(spare);
-      p24_wait_quiet(spare, 0);
-    }
-    __syncwarp();
   } else {
+    // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
     const int q = warp & 3;
     uint32_t tl = 0;
     for (int t = cid; t < p.num_tiles; t += ncl, ++tl) {
@@ -808,7 +829,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
         continue;
       }
       ta = 2 * ta + rank;
@@ -851,14 +872,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
     }
   }
 
   tc_fence_before();
-  cluster_sync();  // the peer may still multicast into / arrive on this CTA until here
+  cluster_sync();  // the peer may still signal this CTA's barriers until here
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
 }
 
 // ---------------------------------------------------------------- host side
@@ -970,7 +992,7 @@ int num_sms() {
 constexpr int kSpBNWide = 256;
 constexpr int kSpBNOverlap = 192;
 constexpr int kSpStages = 4;
-constexpr int kDwStages = 4;
+constexpr int kDwStages = 6;
 
 template <int BN, bool kTrans, int kEpi>
 cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const CUtensorMap& l,
