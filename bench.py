@@ -391,7 +391,7 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize(dev)
             return c0.elapsed_time(c1) / args.steps
 
-        for key in ("gpt2", "1p3b", "7b_act24", "70b_m2048", "70b_m8192"):
+        for key in ("gpt2", "1p3b", "7b_act24", "70b_m2048", "70b_m8192", "70b_tail"):
             cw = WORKLOADS[key]
             ci = ffn_inputs(cw, seed=seed, device=dev, bias=False)
             cws = torch.empty(P.ffn24_workspace_size(cw.M, cw.d, cw.ffn, cw.act24), dtype=torch.uint8, device=dev)

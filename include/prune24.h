@@ -33,6 +33,11 @@
  *     NaN sorts above inf); equal magnitudes go to the lower index.
  *   - The library is stateless apart from one device status word per GPU,
  *     written by kernels whose bounded waits expired (see p24_query_status).
+ *   - The device addresses of the library's file-scope arrays (the status word,
+ *     the scratch of p24_colsum_noalloc) are looked up once per device and kept
+ *     for the life of the process. Resetting a device (cudaDeviceReset) after a
+ *     call of this library ran on it is not supported: later calls would use
+ *     the old context's addresses.
  */
 #ifndef PRUNE24_H
 #define PRUNE24_H
@@ -356,6 +361,10 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
  *     dL_down = dY^T T_dn;  dR_down = U_dn^T H;  dL_up = dH^T T_up;  dR_up = U_up^T X
  *   (T and U rounded to bf16). r > 0, r % 8 == 0; the workspace size then comes
  *   from ffn24_workspace_size_lowrank.
+ * dH (optional): device bf16 [M, ffn] (row stride ffn). Where given, the step
+ *   stores the gated hidden gradient dH (the bf16 operand of dX and dW_up) there
+ *   instead of in the workspace, so the caller can read it afterwards. NULL: the
+ *   workspace holds it.
  */
 typedef struct {
   int64_t M, d, ffn;
@@ -387,6 +396,7 @@ typedef struct {
   void* dR_up;
   void* dL_down;
   void* dR_down;
+  void* dH;
 } p24_ffn_args;
 
 /* Device workspace ffn24_step needs for these sizes (compressed weights, dH, ...). */

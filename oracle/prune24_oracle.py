@@ -19,7 +19,7 @@ Sources (web pages on N:M sparse training; cited by title and section):
             "Trainingsstrategie": ReLU as the FFN activation.
 
 The pages give no formula, tie rule, bit encoding or precision. The readings
-used here (each one is listed with its reason in the design notes):
+used here, each the plainest one the rest of the pages supports:
   * magnitude of a bf16 value = its 15 low bits as an unsigned integer
     (exact order of |w| for finite values and inf; NaN sorts above inf;
     +0 and -0 tie);

@@ -14,8 +14,7 @@ Sources (web pages on N:M sparse training; cited by title and section):
 
 No page gives the V:N:M layout, its parameters or how the columns are chosen.
 The readings used here, each the plainest one that fits "N:M on the tensor
-core's 2:4 pattern with a vector-wise selection on top", and each listed in the
-design notes:
+core's 2:4 pattern with a vector-wise selection on top":
   * A [R, C] is sparse along C, its contiguous (reduction) axis. C is a multiple
     of M, and M is a multiple of 4 (M = 4 is plain 2:4).
   * Rows are taken in blocks of V (the last block may be shorter). In each block

@@ -44,7 +44,7 @@ class p24_ffn_args(C.Structure):
                 ("down_fwd", C.POINTER(p24_sparse)), ("down_bwdT", C.POINTER(p24_sparse)),
                 ("W_down_masked", C.c_void_p), ("r", C.c_int64), ("L_up", C.c_void_p), ("R_up", C.c_void_p),
                 ("L_down", C.c_void_p), ("R_down", C.c_void_p), ("dL_up", C.c_void_p), ("dR_up", C.c_void_p),
-                ("dL_down", C.c_void_p), ("dR_down", C.c_void_p)]
+                ("dL_down", C.c_void_p), ("dR_down", C.c_void_p), ("dH", C.c_void_p)]
 
 
 def _load() -> C.CDLL:
@@ -405,7 +405,8 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     masks) and W_up / W_down are not read (they may be None).
     adapters: optional SLOPE low-rank adapters, a dict of bf16 tensors L_up [ffn, r],
     R_up [r, d], L_down [d, r], R_down [r, ffn]; their gradients come back as
-    dL_up, dR_up, dL_down, dR_down (see include/prune24.h)."""
+    dL_up, dR_up, dL_down, dR_down (see include/prune24.h).
+    A bf16 [M, ffn] tensor under out["dH"] receives the gated hidden gradient dH."""
     M, d, _ = _mat(X, name="X")
     w = dict(weights or {})
     if keep_masks:
@@ -453,6 +454,11 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     for k, st in structs.items():
         setattr(a, k, C.pointer(st))
     a.W_down_masked = _ptr(w.get("W_down_masked"))
+    if o.get("dH") is not None:
+        _mat(o["dH"], name="dH")
+        if tuple(o["dH"].shape) != (M, ffn) or not o["dH"].is_contiguous():
+            raise ValueError(f"dH must be a contiguous {(M, ffn)} tensor")
+        a.dH = o["dH"].data_ptr()
     if r:
         a.r = r
         for k in ("L_up", "R_up", "L_down", "R_down"):

@@ -408,6 +408,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   }
   if (keep && act24 && !a->W_down_masked) return P24_EINVAL;
   if (a->W_down_masked) P24_TRY(check_dense(a->W_down_masked, d, ffn, ffn));
+  if (a->dH) P24_TRY(check_dense(a->dH, M, ffn, ffn));
   const bool ad = (a->flags & P24_STEP_ADAPTERS) != 0;
   const int64_t r = a->r;
   if (ad) {
@@ -465,6 +466,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   if (a->down_fwd) L.dn_fwd = *a->down_fwd;
   if (a->down_bwdT) L.dn_bwdT = *a->down_bwdT;
   if (a->W_down_masked) wdm = a->W_down_masked;
+  if (a->dH) dHv = a->dH;
   // 1. fresh 2:4 masks of both weights, and their double-pruned transposes (GMP);
   //    with fixed masks the caller's compressed weights are used as they are
   //    (with adapters, also the transposed factors their backward products need)

@@ -20,7 +20,9 @@ int64_t colsum_slabs(int64_t M);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s);
 // Same sums with the library's fixed device scratch instead of a caller workspace.
-constexpr int64_t kNoAllocColsumScratch = int64_t(1) << 20;  // floats (4 MiB per GPU)
+constexpr int64_t kNoAllocColsumScratch = P24_COLSUM_NOALLOC_SCRATCH_FLOATS;  // floats (4 MiB per GPU)
+static_assert(P24_COLSUM_NOALLOC_MAX_COLS <= P24_COLSUM_NOALLOC_SCRATCH_FLOATS,
+              "the widest accepted input needs one row slab of partial sums");
 cudaError_t launch_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, cudaStream_t s);
 
 // ---- tensor-core GEMMs (gemm24_kernels.cu) ----

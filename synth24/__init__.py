@@ -74,6 +74,8 @@ WORKLOADS = {
     "70b_m2048": FFNWorkload("ffn_70b_d8192_ffn28672_M2048", 2048, 8192, 28672, 0.01),
     "70b_m8192": FFNWorkload("ffn_70b_d8192_ffn28672_M8192", 8192, 8192, 28672, 0.01),
     "70b_m16384": FFNWorkload("ffn_70b_d8192_ffn28672_M16384", 16384, 8192, 28672, 0.01),
+    # the 70B tail shapes (M = 1000 tokens, K = 8200, so K % 128 != 0) as one FFN layer
+    "70b_tail": FFNWorkload("ffn_70b_tail_d8200_ffn28672_M1000", 1000, 8200, 28672, 0.01),
 }
 
 
