@@ -272,7 +272,8 @@ def dense_tn(A: np.ndarray, B: np.ndarray):
 
 
 def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
-             H_override: np.ndarray | None = None, adapters: dict | None = None) -> dict:
+             H_override: np.ndarray | None = None, adapters: dict | None = None,
+             act_vnm: tuple | None = None) -> dict:
     """One up -> ReLU -> down FFN layer, forward and backward, all matmuls 2:4.
 
     X [M, d], W_up [ffn, d], W_down [d, ffn], dY [M, d]: bf16 bits; biases fp32.
@@ -294,6 +295,10 @@ def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
       dH and dX gain U_down R_down and U_up R_up (before the gate for dH);
       dL_down = dY^T T_down,  dR_down = U_down^T H_used,
       dL_up = dH^T T_up,      dR_up = U_up^T X             (bf16).
+    act_vnm (optional, V, M): V:N:M activations [TO24 abstract: v:n:m sparsity for the
+    activations]: H is pruned V:2:M along ffn (oracle/vnm_oracle.py) and H_used is its
+    dense form; the rest of the step is unchanged (Y = H_used W_down_pruned^T, the
+    gate is [H_used > 0]).
     """
     ffn, d = W_up.shape
     out: dict = {}
@@ -317,6 +322,12 @@ def ffn_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False,
         Hs_v, Hs_m = compress24(H)
         H_used = decompress24(Hs_v, Hs_m, ffn)
         out.update(Hs_vals=Hs_v, Hs_meta=Hs_m)
+    elif act_vnm is not None:
+        from oracle import vnm_oracle as VNM
+        V, Mg = act_vnm
+        Hv_c, Hv_v, Hv_m = VNM.vnm_compress(H, V, Mg)
+        H_used = VNM.vnm_decompress(Hv_c, Hv_v, Hv_m, H.shape[0], ffn, V, Mg)
+        out.update(Hv_colidx=Hv_c, Hv_vals=Hv_v, Hv_meta=Hv_m)
     else:
         H_used = H
     out["H_used"] = H_used

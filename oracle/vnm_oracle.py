@@ -151,3 +151,21 @@ def vnm_spmm_gathered_f64(X: np.ndarray, colidx: np.ndarray, vals: np.ndarray, m
         cols = (np.arange(G)[:, None] * M + colidx[b].astype(np.int64)).reshape(4 * G)
         Y[:, rows] = Xf[:, cols] @ Wc[rows].T
     return Y
+
+
+def vnm_linear(colidx: np.ndarray, vals: np.ndarray, meta: np.ndarray, R: int, K: int, V: int, M: int,
+               B: np.ndarray, bias: np.ndarray | None = None, relu: bool = False):
+    """Y = act(A . B + bias) with A [R, K] given in V:2:M form (blocks of V rows of A)
+    and B [K, N] dense, bf16 bits: the V:N:M activation A feeding the next linear
+    [TO24 abstract], whose weight W [N, K] is passed transposed as B.
+
+    fp32 accumulation on the decompressed operand; bias and ReLU in fp32 (as for the
+    2:4 GEMMs). Returns (Y_ref fp32 before rounding, Y bf16 bits).
+    """
+    A = vnm_decompress(colidx, vals, meta, R, K, V, M)
+    Y = np.matmul(bf16_to_f32(A), bf16_to_f32(B)).astype(np.float32)
+    if bias is not None:
+        Y = (Y + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+    if relu:
+        Y = np.where(Y > 0, Y, np.float32(0)).astype(np.float32)
+    return Y, f32_to_bf16(Y)

@@ -180,3 +180,90 @@ def test_planted_mistakes_are_caught(ex, monkeypatch):
     monkeypatch.setattr(VNM, "select_columns", real)
     monkeypatch.setattr(VNM, "column_scores", by_column_max)
     assert not check()
+
+
+def test_vnm_linear_on_integers_equals_the_exact_sum():
+    """On small-integer inputs every fp32 partial sum is an exact integer, so
+    vnm_linear(A, B) must equal the int64 product of the decompressed A with B
+    (plus bias, then ReLU), whatever the summation order."""
+    R, K, N, V, M = 40, 64, 24, 16, 8
+    A = ints((R, K), -3, 3, 21)
+    B = ints((K, N), -2, 2, 22)
+    bias = np.arange(N, dtype=np.float32) - 10
+    ci, v, m = VNM.vnm_compress(A, V, M)
+    Ad = O.bf16_to_f32(VNM.vnm_decompress(ci, v, m, R, K, V, M)).astype(np.int64)
+    exact = Ad @ O.bf16_to_f32(B).astype(np.int64) + bias.astype(np.int64)[None, :]
+    Y, Yb = VNM.vnm_linear(ci, v, m, R, K, V, M, B, bias=bias, relu=True)
+    assert np.array_equal(Y, np.maximum(exact, 0).astype(np.float32))
+    assert np.array_equal(O.bf16_to_f32(Yb), Y)          # small integers are exact in bf16
+
+
+def test_vnm_linear_is_the_transposed_gathered_product():
+    """A . B against the kernel-style formulation (gather B's rows per block, 2:4 on
+    the condensed operand) computed in fp64 with the roles of the operands swapped:
+    (A . B)^T = B^T . A^T. Within the fp32 accumulation bound."""
+    R, K, N, V, M = 48, 128, 16, 12, 16
+    rng = np.random.default_rng(23)
+    A = bf(rng.standard_normal((R, K)))
+    B = bf(rng.standard_normal((K, N)))
+    ci, v, m = VNM.vnm_compress(A, V, M)
+    Y, _ = VNM.vnm_linear(ci, v, m, R, K, V, M, B)
+    ref = VNM.vnm_spmm_gathered_f64(np.ascontiguousarray(B.T), ci, v, m, R, K, V, M).T
+    Ad = O.bf16_to_f32(VNM.vnm_decompress(ci, v, m, R, K, V, M)).astype(np.float64)
+    bound = K * 2.0 ** -24 * (np.abs(Ad) @ np.abs(O.bf16_to_f32(B).astype(np.float64)))
+    assert np.all(np.abs(Y - ref) <= bound + 1e-30)
+
+
+def test_vnm_linear_m4_reduces_to_the_2to4_forward():
+    """At M = 4 the V:2:M operand is plain 2:4 along K, so A . B equals the pinned
+    2:4 forward with the roles swapped: spmm24_fwd(B^T, 2:4 of A)^T, bit for bit
+    (both accumulate the same fp32 products with numpy's matmul)."""
+    R, K, N = 20, 32, 12
+    rng = np.random.default_rng(24)
+    A = bf(rng.standard_normal((R, K)))
+    B = bf(rng.standard_normal((K, N)))
+    ci, v, m = VNM.vnm_compress(A, 4, 4)
+    Y, _ = VNM.vnm_linear(ci, v, m, R, K, 4, 4, B)
+    v2, m2 = O.compress24(A)
+    Yt, _ = O.spmm24_fwd(np.ascontiguousarray(B.T), v2, m2, K)
+    np.testing.assert_allclose(Y, Yt.T, rtol=0, atol=K * 2.0 ** -24 * np.abs(Yt).max())
+
+
+def _step_inputs(M, d, ffn, seed):
+    rng = np.random.default_rng(seed)
+    X = bf(rng.standard_normal((M, d)))
+    Wu = bf(0.1 * rng.standard_normal((ffn, d)))
+    Wd = bf(0.1 * rng.standard_normal((d, ffn)))
+    dY = bf(rng.standard_normal((M, d)))
+    return X, Wu, np.zeros(ffn, np.float32), Wd, np.zeros(d, np.float32), dY
+
+
+def test_ffn_step_vnm_at_m4_is_the_act24_step():
+    """V:2:4 keeps all 4 columns of every group, so the V:N:M step reduces to the 2:4
+    activation step (separately pinned) on every output, bit for bit."""
+    args = _step_inputs(48, 32, 64, 31)
+    a = O.ffn_step(*args, act24=True)
+    v = O.ffn_step(*args, act_vnm=(16, 4))
+    for k in ("H_used", "Y", "dH", "dX", "dW_up", "dW_down", "db_up", "db_down"):
+        assert np.array_equal(a[k], v[k]), k
+
+
+def test_ffn_step_vnm_activation_structure_and_chain():
+    """With V:2:8: every row keeps at most 2 values per group of 8, all inside its
+    block's 4 selected columns, each equal to H's value there; the down forward is the
+    plain product of that H_used (so it equals vnm_linear on the transposed weight)."""
+    M, d, ffn, V, Mg = 40, 32, 64, 16, 8
+    X, Wu, bu, Wd, bd, dY = _step_inputs(M, d, ffn, 32)
+    r = O.ffn_step(X, Wu, bu, Wd, bd, dY, act_vnm=(V, Mg))
+    Hu, H = r["H_used"], r["H"]
+    nz = (Hu & np.uint16(0x7FFF)) != 0
+    assert np.all(nz.reshape(M, ffn // Mg, Mg).sum(-1) <= 2)
+    assert np.all(Hu[nz] == H[nz])
+    sel = np.zeros((M, ffn), bool)
+    for m in range(M):
+        for g in range(ffn // Mg):
+            sel[m, g * Mg + r["Hv_colidx"][m // V, g].astype(int)] = True
+    assert not np.any(nz & ~sel)
+    Wm = O.decompress24(r["down_vals"], r["down_meta"], ffn)           # W_down on its 2:4 mask
+    Y, _ = VNM.vnm_linear(r["Hv_colidx"], r["Hv_vals"], r["Hv_meta"], M, ffn, V, Mg, np.ascontiguousarray(Wm.T))
+    np.testing.assert_allclose(Y, r["Y_ref"], rtol=0, atol=ffn * 2.0 ** -24 * np.abs(Y).max())
