@@ -12,9 +12,12 @@ oracle's uses the oracle's. Where the two bf16 operands differ (a rounding that
 fell the other way, or a validated decision on a rounded value), the exact
 products differ by at most |delta| @ |B| (triangle inequality), with delta the
 difference of the two bf16 operands -- known exactly, since both are bf16. That
-term (`chain`, see delta_csr / chained) is added to the elementwise bound; it is
-zero wherever the two sides' operands agree. The intermediates themselves (H,
-dH) are checked against the oracle at the plain tolerance.
+term (`chain`, see delta_csr / chained) is added to the elementwise bound, and the
+relative part of the tolerance is taken of |ref| + chain, the largest magnitude the
+GPU's own product can have (its bf16 rounding scales with that magnitude, not with
+the oracle's). The term is zero wherever the two sides' operands agree. The
+intermediates themselves (H, dH) are checked against the oracle at the plain
+tolerance.
 """
 import numpy as np
 import torch
@@ -48,7 +51,10 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, name: str, chain=None, skip
     normwise = np.linalg.norm(g - r) / (nref if nref > 0 else 1.0)
     bound = ABS_TOL + REL_TOL * np.abs(r)
     if chain is not None:
-        bound = bound + np.asarray(chain, dtype=np.float64)
+        # the GPU's value is the product of its own operand, |value| <= |ref| + chain: its
+        # rounding and summation-order share of the tolerance scales with that magnitude
+        c = np.asarray(chain, dtype=np.float64)
+        bound = bound + (1.0 + REL_TOL) * c
     if extra is not None:
         bound = bound + np.asarray(extra, dtype=np.float64)
     bad = diff > bound
