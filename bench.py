@@ -215,6 +215,79 @@ def cpu_baseline(w, seconds_target: float = 15.0) -> dict:
                        f"median of {len(times)} runs, {t:.2f} s each")}
 
 
+# ------------------------------------------------------------------ hybrid activations
+def bench_hybrid(P, dev, stream, seed, args, peaks) -> dict:
+    """The hybrid ELL + dense-overflow path on synthetic ReLU activations: z ~ N(0, 1)
+    shifted by t = 2.326 (about 1% nonzero), every 50th token by 1.28 (about 10%, so it
+    overflows an ELL of width 256). Shape of the 1.3B FFN: H [8192, 8192], d = 2048.
+    Times the format (HBM-bound stream of H), hybrid -> dense Y = H . W_down^T and
+    dense -> hybrid dH = (dY . W_down) at H's nonzeros (both gather one 4 KB row of
+    W_down^T per nonzero, from L2: W_down^T is 32 MB), beside the dense tensor-core
+    product of the same H for context, and an L2-resident copy as the gather roofline."""
+    from synth24 import normal_bf16
+    R, Cc, N, E = 8192, 8192, 2048, 256
+    z = normal_bf16((R, Cc), 1.0, seed, 7, dev).float()
+    thr = torch.full((R, 1), 2.326, device=dev)
+    thr[::50] = 1.28
+    H = torch.relu(z - thr).to(torch.bfloat16)
+    del z
+    Wt = normal_bf16((Cc, N), 0.02, seed, 3, dev)          # W_down^T [ffn, d]
+    Wd = Wt.t().contiguous()                                # W_down [d, ffn]
+    G = normal_bf16((R, N), 1.0, seed, 6, dev)              # dY
+    h = P.hyb_compress(H, E, R // 16)
+    Y = P.hyb_spmm(h, Wt)
+    S_ell, S_ovf = P.hyb_sddmm(h, G, Wt)
+    Yd = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize(dev)
+    if P.p24_query_status() != 0:
+        raise RuntimeError("device status word set by the hybrid format")
+    nnz = int(h.nnz.sum().item())
+    n_ovf = int(h.n_ovf.item())
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / args.steps
+
+    t_c = timed(lambda: P.hyb_compress(H, E, R // 16, out=h))
+    t_s = timed(lambda: P.hyb_spmm(h, Wt, Y=Y))
+    t_d = timed(lambda: P.hyb_sddmm(h, G, Wt, S_ell=S_ell, S_ovf=S_ovf))
+    t_dense = timed(lambda: P.p24_gemm_nt(H, Wd, C_out=Yd))
+    # L2-resident copy (16 MB each way) as the reference for the gathers
+    a = torch.empty(8 * 2 ** 20, dtype=torch.bfloat16, device=dev)
+    bcopy = torch.empty_like(a)
+    t_l2 = timed(lambda: bcopy.copy_(a))
+    l2_gbs = 2 * a.numel() * 2 / (t_l2 * 1e-3) / 1e9
+    if P.p24_query_status() != 0:
+        raise RuntimeError("device status word set during the hybrid timings")
+    gathered = nnz * N * 2                                   # one row of W_down^T per nonzero
+    c_bytes = R * Cc * 2 + R * E * 4 + R * 8 + n_ovf * Cc * 4
+    out = {"shape": {"tokens": R, "ffn": Cc, "d": N, "E": E, "cap": R // 16},
+           "density": nnz / (R * Cc), "overflow_rows": n_ovf,
+           "compress": {"ms": t_c, "value": c_bytes / (t_c * 1e-3) / 1e9, "unit": "GB/s", "bound": "hbm",
+                        "frac": c_bytes / (t_c * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "algorithmic_bytes": c_bytes},
+           "hybrid_to_dense": {"ms": t_s, "gathered_GBs": gathered / (t_s * 1e-3) / 1e9,
+                               "frac_of_l2_copy": gathered / (t_s * 1e-3) / 1e9 / l2_gbs,
+                               "tflops": 2 * nnz * N / (t_s * 1e-3) / 1e12},
+           "dense_to_hybrid": {"ms": t_d, "gathered_GBs": gathered / (t_d * 1e-3) / 1e9,
+                               "frac_of_l2_copy": gathered / (t_d * 1e-3) / 1e9 / l2_gbs,
+                               "tflops": 2 * nnz * N / (t_d * 1e-3) / 1e12},
+           "dense_tensor_core_same_product_ms": t_dense,
+           "l2_copy_GBs": l2_gbs,
+           "note": "gathered bytes = nonzeros x d x 2 (one W_down^T row per nonzero); the L2 figure is a "
+                   "16 MB copy measured in this run"}
+    del H, Wt, Wd, G, h, Y, S_ell, S_ovf, Yd, a, bcopy
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, world, rank, local):
     import semi_structured_sparse_prune24_gb300 as P
@@ -337,6 +410,79 @@ def run_ours(args, world, rank, local):
                  "unit": "TFLOPS (dense-equivalent, adapter FLOPs included)", "adapter_flop": ad_flop,
                  "overhead_vs_plain_step": ad_ms / ms_step - 1.0}
         del out_ad, ws_ad, ad
+        torch.cuda.empty_cache()
+
+    # ---- V:N:M activations (256:2:8, 75% sparse H): the same step with H pruned V:2:M
+    #      along ffn and the down forward on the V:2:M GEMM (gathered W_down^T rows)
+    vnm = None
+    if not args.no_vnm:
+        try:
+            VV, VM = 256, 8
+            ws_v = torch.empty(P.ffn24_workspace_size(w.M, w.d, w.ffn, vnm=(VV, VM)), dtype=torch.uint8, device=dev)
+            out_v = P.ffn24_step(X, Wu, bu, Wd, bd, dY, workspace=ws_v, vnm=(VV, VM))
+            for _ in range(args.warmup):
+                P.ffn24_step(X, Wu, bu, Wd, bd, dY, out=out_v, workspace=ws_v, vnm=(VV, VM))
+            evv = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nph * args.steps)]
+            for e in evv:
+                e.record(stream)
+            torch.cuda.synchronize(dev)
+            hv = [(ctypes.c_void_p * (2 * nph))(*[evv[i * 2 * nph + j].cuda_event for j in range(2 * nph)])
+                  for i in range(args.steps)]
+            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            v0.record(stream)
+            for i in range(args.steps):
+                P.ffn24_step(X, Wu, bu, Wd, bd, dY, out=out_v, workspace=ws_v, vnm=(VV, VM), events=hv[i])
+            v1.record(stream)
+            torch.cuda.synchronize(dev)
+            if P.p24_query_status() != 0:
+                raise RuntimeError("device status word set during the V:N:M steps")
+            vms = v0.elapsed_time(v1) / args.steps
+            vph = [statistics.mean(evv[i * 2 * nph + 2 * q].elapsed_time(evv[i * 2 * nph + 2 * q + 1])
+                                   for i in range(args.steps)) for q in range(nph)]
+            down_ms = vph[3]
+            kc = 4 * w.ffn // VM                     # condensed reduction length of the down GEMM
+            executed = 2 * w.M * w.d * kc             # dense-equivalent FLOP of the condensed product
+            vnm = {"V": VV, "M": VM, "ms_per_step": vms, "value": flop / (vms * 1e-3) / 1e12,
+                   "unit": "TFLOPS (dense-equivalent of the dense FFN step)",
+                   "speedup_vs_2to4_step": ms_step / vms, "phase_ms": dict(zip(P.STEP_PHASE_NAMES, vph)),
+                   "down_gemm": {"kernel": "spmm_kernel gathered-B (vnm24_spmm)", "ms": down_ms,
+                                 "dense_equiv_tflops": gemm_flop / (down_ms * 1e-3) / 1e12,
+                                 "achieved": executed / (down_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                 "peak": sparse_peak, "frac": executed / (down_ms * 1e-3) / 1e12 / sparse_peak,
+                                 "note": "achieved counts the condensed product 2*M*d*(4*ffn/M_group) at the "
+                                         "2:4 sparse rate; dense_equiv counts 2*M*d*ffn"}}
+            del out_v, ws_v
+            # the V:2:M prune of an H-shaped activation, masked in place, on its own
+            Hv = torch.relu(normal_bf16((w.M, w.ffn), 1.0, seed, 7, dev))
+            ci, hs = P.vnm24_compress(Hv, VV, VM)
+            for _ in range(args.warmup):
+                P.vnm24_compress(Hv, VV, VM, out=hs, colidx=ci, A_masked=Hv)
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            p0.record(stream)
+            for _ in range(args.steps):
+                P.vnm24_compress(Hv, VV, VM, out=hs, colidx=ci, A_masked=Hv)
+            p1.record(stream)
+            torch.cuda.synchronize(dev)
+            pms = p0.elapsed_time(p1) / args.steps
+            per_elt = 2 + 2 + 4 / VM * 0.5 + 4 / VM / 8 + 4 / (VV * VM)   # read, masked write, values, nibbles, offsets
+            gbs = per_elt * Hv.numel() / (pms * 1e-3) / 1e9
+            vnm["prune_H"] = {"ms": pms, "value": gbs, "unit": "GB/s", "frac_hbm": gbs / peaks["hbm_gbs"],
+                              "algorithmic_bytes_per_elt": per_elt, "shape": [w.M, w.ffn]}
+            del Hv, ci, hs
+        except Exception as exc:  # a failure here must not cost the bench line
+            vnm = {"error": f"{type(exc).__name__}: {exc}"}
+        torch.cuda.empty_cache()
+
+    # ---- hybrid ELL + dense-overflow activations: format and its two training products
+    #      on the 1.3B FFN shape (8192 tokens x 8192 hidden units, d = 2048)
+    hyb = None
+    if not args.no_hybrid:
+        try:
+            hyb = bench_hybrid(P, dev, stream, seed, args, peaks)
+        except Exception as exc:  # a failure here must not cost the bench line
+            hyb = {"error": f"{type(exc).__name__}: {exc}"}
         torch.cuda.empty_cache()
 
     # ---- a short step (GPT-2-size FFN), eager against a CUDA-graph replay: the
@@ -555,6 +701,8 @@ def run_ours(args, world, rank, local):
             "kernels": breakdown,
             "roofline": roofline,
             "slope_adapters": slope,
+            "vnm_activations": vnm,
+            "hybrid_activations": hyb,
             "graphs": graphs,
             "configs": configs,
             "prune": prune,
@@ -610,6 +758,8 @@ def main():
     ap.add_argument("--no-adapters", action="store_true")
     ap.add_argument("--no-graphs", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-vnm", action="store_true")
+    ap.add_argument("--no-hybrid", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -56,7 +56,8 @@ typedef enum {
   P24_ECUDA = -3,         /* a CUDA runtime/driver call or launch failed */
   P24_ETIMEOUT = -4,      /* a kernel's bounded wait expired (device status word) */
   P24_EUNSUPPORTED = -5,  /* no sm_103a device, or a shape outside the supported set */
-  P24_ENOSPACE = -6       /* workspace smaller than required */
+  P24_ENOSPACE = -6,      /* workspace smaller than required */
+  P24_ECAPACITY = -7      /* a data-dependent output exceeded its capacity (device status word) */
 } p24_status;
 
 /*
@@ -136,12 +137,39 @@ int prune24_transpose_repack(const p24_sparse* fwd, const p24_sparse* bwdT,
  *   out    : descriptor of the condensed matrix, rows = rows, cols = 4*cols/M:
  *            row r, group g holds A's values at the 4 kept columns of g in the
  *            2:4 format of prune24_compress (values, nibbles, padding).
+ *   A_masked : optional device bf16 [rows, ldam]: A with every pruned entry set
+ *            to +0 (the dense form of the V:2:M matrix). It may be A itself
+ *            (in place, ldam == lda). Needs V <= 256 and cols % 8 == 0
+ *            (P24_EUNSUPPORTED otherwise). NULL to skip.
  * Returns P24_EINVAL for bad V, M, shapes or null pointers, P24_EALIGN for
  * misaligned A or out; nothing is launched then.
  */
 int vnm24_compress(const void* A, int64_t rows, int64_t cols, int64_t lda,
                    int64_t V, int64_t M, uint8_t* colidx, const p24_sparse* out,
-                   void* stream);
+                   void* A_masked, int64_t ldam, void* stream);
+
+/*
+ * vnm24_spmm -- Y = act(A . B + bias) with A V:2:M-sparse, as vnm24_compress
+ * writes it, and B dense with its reduction axis outermost (V:N:M activations
+ * feeding the next FFN matmul: "To 2:4 Sparsity and Beyond", abstract; the
+ * VENOM format of the ESPLAG success story, "Solution").
+ *   colidx, A : vnm24_compress's outputs for an [R, K] matrix pruned with V and
+ *            M (A->rows = R, A->cols = 4 K / M).
+ *   B      : device bf16 [K, ldb], N columns, read only (for Y = A W^T, the
+ *            weight W [N, K] stored transposed).
+ *   bias   : device fp32 [N] with P24_EPI_BIAS; flags: P24_EPI_BIAS | P24_EPI_RELU.
+ *   Y      : device bf16 [R, ldy], N columns; fp32 accumulation, one rounding.
+ * Each block of V rows multiplies, per group of M, the 4 rows of B its colidx
+ * selects (fetched by TMA gather), and the sparse tensor cores skip the 2 pruned
+ * values of every 4: the result is the dense product of A's decompressed form and
+ * B, up to the order of the fp32 sums.
+ * Supported shapes (P24_EUNSUPPORTED otherwise): V a multiple of 256 (a CTA pair's
+ * 256 rows share one selection), A->cols a multiple of 128 (K a multiple of 32 M),
+ * N a multiple of 256. colidx must be 16-byte aligned (P24_EALIGN).
+ */
+int vnm24_spmm(const uint8_t* colidx, const p24_sparse* A, int64_t V, int64_t M,
+               const void* B, int64_t N, int64_t ldb, const float* bias,
+               uint32_t flags, void* Y, int64_t ldy, void* stream);
 
 /*
  * prune24_compress_both -- prune24_compress followed by
@@ -316,10 +344,61 @@ int p24_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out,
 #define P24_COLSUM_NOALLOC_MAX_COLS P24_COLSUM_NOALLOC_SCRATCH_FLOATS
 int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, void* stream);
 
+/*
+ * Hybrid ELL + dense-overflow activations ("Sparser, Faster, Lighter Transformer
+ * Language Models", "Methodologie": for training, rows with few nonzeros are held in
+ * a compact ELL matrix and rows with many -- overflows -- in a dense backup matrix;
+ * custom kernels multiply hybrid by dense and dense into hybrid). The page gives no
+ * layout; this is the one used here. A [rows, cols] bf16, a value is nonzero when its
+ * magnitude bits are not 0 (-0 is zero):
+ *   nnz      : device int32 [rows], the nonzero count of each row.
+ *   ell_cols : device uint16 [rows, E]; ell_vals : device bf16 [rows, E]. A row with
+ *              nnz <= E keeps its nonzero columns in ascending order and their values;
+ *              the other slots (and every slot of an overflow row) hold column 0, +0.
+ *   slot     : device int32 [rows]: -1 for an ELL row, else the row's rank among the
+ *              overflow rows (nnz > E), in row order.
+ *   ovf_rows : device int32 [cap], the overflow rows by slot (-1 past their count).
+ *   n_ovf    : device int32 [1], the number of overflow rows (it may exceed cap).
+ *   ovf      : device bf16 [cap, ldo]: backup row k = overflow row ovf_rows[k] as it is.
+ * E >= 1; cols <= 65536 and cols % 8 == 0; cap >= 0. 16-byte aligned pointers, except
+ * nnz, slot, ovf_rows, n_ovf (4-byte). More overflow rows than cap is an error found on
+ * the device: the rows past the capacity are not stored, the products write zeros for
+ * them, and P24_ECAPACITY is left in the status word (p24_query_status).
+ */
+typedef struct {
+  int64_t rows, cols, E, cap;
+  int32_t* nnz;
+  uint16_t* ell_cols;
+  void* ell_vals;
+  int32_t* slot;
+  int32_t* ovf_rows;
+  int32_t* n_ovf;
+  void* ovf;
+  int64_t ldo;
+} p24_hybrid;
+
+/* hyb_compress -- the hybrid form of A (device bf16 [h->rows, lda], h->cols columns),
+ * written into h's buffers (caller-owned). Integer work: a pure function of A's bits. */
+int hyb_compress(const void* A, int64_t lda, const p24_hybrid* h, void* stream);
+
+/* hyb_spmm -- hybrid to dense: Y = A . B, A in hybrid form [rows, cols], B device bf16
+ * [cols, ldb] with N columns (e.g. W_down^T for the down projection, W_up for the input
+ * gradient), Y device bf16 [rows, ldy]; fp32 accumulation, one rounding. N % 8 == 0. */
+int hyb_spmm(const p24_hybrid* h, const void* B, int64_t N, int64_t ldb, void* Y, int64_t ldy, void* stream);
+
+/* hyb_sddmm -- dense to hybrid: S = (G . B^T) at A's nonzero positions, in A's hybrid
+ * layout (dH = (dY W_down) * [H != 0] with G = dY, B = W_down^T). G device bf16
+ * [rows, ldg], B device bf16 [cols, ldb], both N columns (N % 8 == 0). Outputs:
+ * S_ell bf16 [rows, E] (values in A's ELL slots, +0 padding) and S_ovf bf16 [cap, lds]
+ * (backup rows: values at A's nonzeros, +0 elsewhere). fp32 accumulation. */
+int hyb_sddmm(const p24_hybrid* h, const void* G, int64_t N, int64_t ldg, const void* B, int64_t ldb,
+              void* S_ell, void* S_ovf, int64_t lds, void* stream);
+
 /* Flags of ffn24_step. */
 #define P24_STEP_ACT24 0x1u /* 2:4-prune ReLU(up) and feed it as the sparse operand of down */
 #define P24_STEP_KEEP_MASKS 0x2u /* use the caller's compressed weights as they are (fixed masks) */
 #define P24_STEP_ADAPTERS 0x4u /* SLOPE's low-rank adapters on both linears (rank r) */
+#define P24_STEP_VNM 0x8u /* V:2:M-prune ReLU(up) along ffn and feed it to the down GEMM (vnm24_spmm) */
 
 /*
  * One FFN layer (up -> ReLU -> down), forward and backward, every matmul 2:4
@@ -365,6 +444,17 @@ int p24_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t ldg, float* 
  *   stores the gated hidden gradient dH (the bf16 operand of dX and dW_up) there
  *   instead of in the workspace, so the caller can read it afterwards. NULL: the
  *   workspace holds it.
+ * V:N:M activations (P24_STEP_VNM; "To 2:4 Sparsity and Beyond", abstract: v:n:m
+ *   sparsity for the activations): H is pruned V:2:M along ffn by vnm24_compress's
+ *   rule with V = vnm_V and M = vnm_M, in place (the H output is the pruned H), and
+ *   the down forward runs on the sparse tensor cores as vnm24_spmm with W_down on
+ *   its 2:4 mask, transposed, as the gathered operand:
+ *     H = V:2:M(ReLU(X W_up^T + b_up));  Y = H W_down^T + b_down;
+ *   the backward is the one above with this H (the gate [H > 0] is the V:2:M mask
+ *   times the ReLU gate). Requires vnm_V = 256, vnm_M in {4, 8, ..., 128},
+ *   ffn % (32 vnm_M) == 0 and d % 256 == 0; not with P24_STEP_ACT24 or
+ *   P24_STEP_ADAPTERS (P24_EUNSUPPORTED). The workspace size comes from
+ *   ffn24_workspace_size_args.
  */
 typedef struct {
   int64_t M, d, ffn;
@@ -397,10 +487,15 @@ typedef struct {
   void* dL_down;
   void* dR_down;
   void* dH;
+  int64_t vnm_V;
+  int64_t vnm_M;
 } p24_ffn_args;
 
 /* Device workspace ffn24_step needs for these sizes (compressed weights, dH, ...). */
 size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags);
+/* The same for the step described by a (M, d, ffn, flags, r, vnm_V, vnm_M are read):
+ * covers every flag, P24_STEP_VNM included. 0 for invalid sizes. */
+size_t ffn24_workspace_size_args(const p24_ffn_args* a);
 /* The same with low-rank adapters of rank r (flags with P24_STEP_ADAPTERS). */
 size_t ffn24_workspace_size_lowrank(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r);
 int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream);

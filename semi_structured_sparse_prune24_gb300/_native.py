@@ -17,11 +17,13 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libprune24.so")
 
 P24_OK, P24_EINVAL, P24_EALIGN, P24_ECUDA, P24_ETIMEOUT, P24_EUNSUPPORTED, P24_ENOSPACE = 0, -1, -2, -3, -4, -5, -6
+P24_ECAPACITY = -7
 P24_EPI_BIAS, P24_EPI_RELU, P24_EPI_ACT24 = 0x1, 0x2, 0x4
 P24_EPI_TEST_STALL = 0x80000000
 P24_STEP_ACT24 = 0x1
 P24_STEP_KEEP_MASKS = 0x2
 P24_STEP_ADAPTERS = 0x4
+P24_STEP_VNM = 0x8
 
 
 class P24Error(RuntimeError):
@@ -44,7 +46,14 @@ class p24_ffn_args(C.Structure):
                 ("down_fwd", C.POINTER(p24_sparse)), ("down_bwdT", C.POINTER(p24_sparse)),
                 ("W_down_masked", C.c_void_p), ("r", C.c_int64), ("L_up", C.c_void_p), ("R_up", C.c_void_p),
                 ("L_down", C.c_void_p), ("R_down", C.c_void_p), ("dL_up", C.c_void_p), ("dR_up", C.c_void_p),
-                ("dL_down", C.c_void_p), ("dR_down", C.c_void_p), ("dH", C.c_void_p)]
+                ("dL_down", C.c_void_p), ("dR_down", C.c_void_p), ("dH", C.c_void_p), ("vnm_V", C.c_int64),
+                ("vnm_M", C.c_int64)]
+
+
+class p24_hybrid(C.Structure):
+    _fields_ = [("rows", C.c_int64), ("cols", C.c_int64), ("E", C.c_int64), ("cap", C.c_int64),
+                ("nnz", C.c_void_p), ("ell_cols", C.c_void_p), ("ell_vals", C.c_void_p), ("slot", C.c_void_p),
+                ("ovf_rows", C.c_void_p), ("n_ovf", C.c_void_p), ("ovf", C.c_void_p), ("ldo", C.c_int64)]
 
 
 def _load() -> C.CDLL:
@@ -60,7 +69,8 @@ def _load() -> C.CDLL:
         "prune24_compress": (i32, [vp, i64, i64, i64, sp, vp, i64, vp]),
         "prune24_transpose_repack": (i32, [sp, sp, vp]),
         "prune24_compress_both": (i32, [vp, i64, i64, i64, sp, sp, vp, i64, vp]),
-        "vnm24_compress": (i32, [vp, i64, i64, i64, i64, i64, vp, sp, vp]),
+        "vnm24_compress": (i32, [vp, i64, i64, i64, i64, i64, vp, sp, vp, i64, vp]),
+        "vnm24_spmm": (i32, [vp, sp, i64, i64, vp, i64, i64, vp, u32, vp, i64, vp]),
         "spmm24_fwd": (i32, [vp, i64, i64, sp, vp, u32, vp, i64, sp, vp]),
         "spmm24_fwd_sparse_act": (i32, [sp, vp, i64, i64, vp, u32, vp, i64, vp]),
         "spmm24_bwd_dx": (i32, [vp, i64, i64, sp, vp, i64, vp, i64, vp, vp]),
@@ -75,8 +85,12 @@ def _load() -> C.CDLL:
         "p24_colsum_noalloc": (i32, [vp, i64, i64, i64, vp, vp]),
         "ffn24_workspace_size": (sz, [i64, i64, i64, u32]),
         "ffn24_workspace_size_lowrank": (sz, [i64, i64, i64, u32, i64]),
+        "ffn24_workspace_size_args": (sz, [C.POINTER(p24_ffn_args)]),
         "ffn24_step": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp]),
         "ffn24_step_traced": (i32, [C.POINTER(p24_ffn_args), vp, sz, vp, C.POINTER(vp), i32]),
+        "hyb_compress": (i32, [vp, i64, C.POINTER(p24_hybrid), vp]),
+        "hyb_spmm": (i32, [C.POINTER(p24_hybrid), vp, i64, i64, vp, i64, vp]),
+        "hyb_sddmm": (i32, [C.POINTER(p24_hybrid), vp, i64, i64, vp, i64, vp, vp, i64, vp]),
         "p24_launch_count": (C.c_uint64, []),
         "p24_query_status": (i32, [vp]),
         "p24_query_timeout": (i32, [vp, C.POINTER(i64), C.POINTER(i64)]),
@@ -186,9 +200,11 @@ def prune24_transpose_repack(fwd: Sparse24, bwdT: Sparse24 | None = None, stream
 
 
 def vnm24_compress(A: torch.Tensor, V: int, M: int, out: Sparse24 | None = None,
-                   colidx: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, Sparse24]:
+                   colidx: torch.Tensor | None = None, A_masked: torch.Tensor | None = None,
+                   stream=None) -> tuple[torch.Tensor, Sparse24]:
     """V:2:M prune of A along its columns: (colidx uint8 [ceil(rows/V), cols/M, 4],
-    the condensed [rows, 4 cols/M] matrix compressed 2:4)."""
+    the condensed [rows, 4 cols/M] matrix compressed 2:4). A_masked (optional, may be
+    A itself) receives A with the pruned entries set to +0."""
     rows, cols, lda = _mat(A, name="A")
     if M <= 0 or cols % M:
         raise P24Error(P24_EINVAL, f"vnm24_compress: cols={cols} is not a multiple of M={M}")
@@ -196,10 +212,29 @@ def vnm24_compress(A: torch.Tensor, V: int, M: int, out: Sparse24 | None = None,
     out = Sparse24.empty(rows, 4 * (cols // M), A.device) if out is None else out
     if colidx is None:
         colidx = torch.empty((nb, cols // M, 4), dtype=torch.uint8, device=A.device)
+    ldam = 0
+    if A_masked is not None:
+        _, _, ldam = _mat(A_masked, name="A_masked")
     d = out.c()
-    _check(lib.vnm24_compress(A.data_ptr(), rows, cols, lda, V, M, colidx.data_ptr(), C.byref(d), _stream(stream)),
-           "vnm24_compress")
+    _check(lib.vnm24_compress(A.data_ptr(), rows, cols, lda, V, M, colidx.data_ptr(), C.byref(d), _ptr(A_masked),
+                              ldam, _stream(stream)), "vnm24_compress")
     return colidx, out
+
+
+def vnm24_spmm(colidx: torch.Tensor, A: Sparse24, V: int, M: int, B: torch.Tensor, bias: torch.Tensor | None = None,
+               relu: bool = False, Y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = act(A . B + bias): A V:2:M-sparse (vnm24_compress's colidx and condensed
+    matrix, pruned with V and M), B dense [K, N] with K = A.cols * M / 4."""
+    K, N, ldb = _mat(B, name="B")
+    if K != A.cols // 4 * M:
+        raise ValueError(f"B has {K} rows; the V:2:M operand needs {A.cols // 4 * M}")
+    Y = torch.empty((A.rows, N), dtype=torch.bfloat16, device=B.device) if Y is None else Y
+    _, _, ldy = _mat(Y, name="Y")
+    flags = (P24_EPI_BIAS if bias is not None else 0) | (P24_EPI_RELU if relu else 0)
+    a = A.c()
+    _check(lib.vnm24_spmm(colidx.data_ptr(), C.byref(a), V, M, B.data_ptr(), N, ldb, _ptr(bias), flags,
+                          Y.data_ptr(), ldy, _stream(stream)), "vnm24_spmm")
+    return Y
 
 
 def prune24_compress_both(W: torch.Tensor, fwd: Sparse24 | None = None, bwdT: Sparse24 | None = None,
@@ -379,7 +414,11 @@ def ffn24_workspace_size_lowrank(M: int, d: int, ffn: int, act24: bool, r: int) 
     return int(lib.ffn24_workspace_size_lowrank(M, d, ffn, (P24_STEP_ACT24 if act24 else 0) | P24_STEP_ADAPTERS, r))
 
 
-def ffn24_workspace_size(M: int, d: int, ffn: int, act24: bool = False) -> int:
+def ffn24_workspace_size(M: int, d: int, ffn: int, act24: bool = False, vnm: tuple | None = None) -> int:
+    if vnm:
+        a = p24_ffn_args(M=M, d=d, ffn=ffn, flags=P24_STEP_VNM | (P24_STEP_ACT24 if act24 else 0),
+                         vnm_V=int(vnm[0]), vnm_M=int(vnm[1]))
+        return int(lib.ffn24_workspace_size_args(C.byref(a)))
     return int(lib.ffn24_workspace_size(M, d, ffn, P24_STEP_ACT24 if act24 else 0))
 
 
@@ -393,7 +432,7 @@ STEP_WEIGHTS = ("up_fwd", "up_bwdT", "down_fwd", "down_bwdT")
 
 def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict | None = None,
                workspace: torch.Tensor | None = None, stream=None, events=None, weights: dict | None = None,
-               keep_masks: bool = False, adapters: dict | None = None) -> dict:
+               keep_masks: bool = False, adapters: dict | None = None, vnm: tuple | None = None) -> dict:
     """One 2:4 FFN layer fwd+bwd; returns dict(Y, H, dX, dW_up, dW_down, db_up, db_down).
 
     events: optional ctypes array of 2 * STEP_PHASES raw cudaEvent_t handles, recorded
@@ -406,7 +445,9 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
     adapters: optional SLOPE low-rank adapters, a dict of bf16 tensors L_up [ffn, r],
     R_up [r, d], L_down [d, r], R_down [r, ffn]; their gradients come back as
     dL_up, dR_up, dL_down, dR_down (see include/prune24.h).
-    A bf16 [M, ffn] tensor under out["dH"] receives the gated hidden gradient dH."""
+    A bf16 [M, ffn] tensor under out["dH"] receives the gated hidden gradient dH.
+    vnm: (V, M) for V:N:M activations (P24_STEP_VNM): H is pruned V:2:M along ffn and
+    the down forward runs as vnm24_spmm; the returned H is the pruned one."""
     M, d, _ = _mat(X, name="X")
     w = dict(weights or {})
     if keep_masks:
@@ -441,15 +482,17 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
             if t.dtype != bf or tuple(t.shape) != shape or not t.is_contiguous():
                 raise ValueError(f"adapter {k} must be a contiguous bf16 {shape} tensor")
             o.setdefault("d" + k, torch.empty(shape, dtype=bf, device=dev))
-    need = ffn24_workspace_size_lowrank(M, d, ffn, act24, r) if r else ffn24_workspace_size(M, d, ffn, act24)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     flags = ((P24_STEP_ACT24 if act24 else 0) | (P24_STEP_KEEP_MASKS if keep_masks else 0) |
-             (P24_STEP_ADAPTERS if r else 0))
+             (P24_STEP_ADAPTERS if r else 0) | (P24_STEP_VNM if vnm else 0))
     a = p24_ffn_args(M, d, ffn, flags, X.data_ptr(), _ptr(W_up), _ptr(b_up),
                      _ptr(W_down), _ptr(b_down), dY.data_ptr(), o["Y"].data_ptr(), o["H"].data_ptr(),
                      o["dX"].data_ptr(), o["dW_up"].data_ptr(), o["dW_down"].data_ptr(), _ptr(o["db_up"]),
                      _ptr(o["db_down"]))
+    a.r = r
+    if vnm:
+        a.vnm_V, a.vnm_M = int(vnm[0]), int(vnm[1])
+    if workspace is None:
+        workspace = torch.empty(int(lib.ffn24_workspace_size_args(C.byref(a))), dtype=torch.uint8, device=dev)
     structs = {k: w[k].c() for k in STEP_WEIGHTS if w.get(k) is not None}  # alive for the call
     for k, st in structs.items():
         setattr(a, k, C.pointer(st))
@@ -460,7 +503,6 @@ def ffn24_step(X, W_up, b_up, W_down, b_down, dY, act24: bool = False, out: dict
             raise ValueError(f"dH must be a contiguous {(M, ffn)} tensor")
         a.dH = o["dH"].data_ptr()
     if r:
-        a.r = r
         for k in ("L_up", "R_up", "L_down", "R_down"):
             setattr(a, k, adapters[k].data_ptr())
             setattr(a, "d" + k, o["d" + k].data_ptr())
@@ -492,3 +534,67 @@ def p24_query_timeout(stream=None) -> tuple[int, int, int]:
 def p24_query_status(stream=None) -> int:
     """Synchronise the stream; return (and clear) the device status word."""
     return int(lib.p24_query_status(_stream(stream)))
+
+
+@dataclass
+class Hybrid:
+    """Hybrid ELL + dense-overflow form of a [rows, cols] bf16 matrix (see p24_hybrid in
+    include/prune24.h): device tensors nnz, ell_cols, ell_vals, slot, ovf_rows, n_ovf, ovf."""
+    nnz: torch.Tensor
+    ell_cols: torch.Tensor
+    ell_vals: torch.Tensor
+    slot: torch.Tensor
+    ovf_rows: torch.Tensor
+    n_ovf: torch.Tensor
+    ovf: torch.Tensor
+    rows: int
+    cols: int
+    E: int
+    cap: int
+
+    @staticmethod
+    def empty(rows: int, cols: int, E: int, cap: int, device="cuda") -> "Hybrid":
+        i32 = torch.int32
+        return Hybrid(torch.empty(rows, dtype=i32, device=device),
+                      torch.empty((rows, E), dtype=torch.int16, device=device),   # uint16 column bits
+                      torch.empty((rows, E), dtype=torch.bfloat16, device=device),
+                      torch.empty(rows, dtype=i32, device=device), torch.empty(max(cap, 1), dtype=i32, device=device),
+                      torch.empty(1, dtype=i32, device=device),
+                      torch.empty((max(cap, 1), cols), dtype=torch.bfloat16, device=device), rows, cols, E, cap)
+
+    def c(self) -> p24_hybrid:
+        return p24_hybrid(self.rows, self.cols, self.E, self.cap, self.nnz.data_ptr(), self.ell_cols.data_ptr(),
+                          self.ell_vals.data_ptr(), self.slot.data_ptr(), self.ovf_rows.data_ptr(),
+                          self.n_ovf.data_ptr(), self.ovf.data_ptr(), self.ovf.stride(0))
+
+
+def hyb_compress(A: torch.Tensor, E: int, cap: int, out: Hybrid | None = None, stream=None) -> Hybrid:
+    """The hybrid form of A (ELL width E, backup capacity cap)."""
+    rows, cols, lda = _mat(A, name="A")
+    out = Hybrid.empty(rows, cols, E, cap, A.device) if out is None else out
+    h = out.c()
+    _check(lib.hyb_compress(A.data_ptr(), lda, C.byref(h), _stream(stream)), "hyb_compress")
+    return out
+
+
+def hyb_spmm(h: Hybrid, B: torch.Tensor, Y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Hybrid to dense: Y = A . B, B [cols, N]."""
+    K, N, ldb = _mat(B, name="B")
+    Y = torch.empty((h.rows, N), dtype=torch.bfloat16, device=B.device) if Y is None else Y
+    _, _, ldy = _mat(Y, name="Y")
+    hc = h.c()
+    _check(lib.hyb_spmm(C.byref(hc), B.data_ptr(), N, ldb, Y.data_ptr(), ldy, _stream(stream)), "hyb_spmm")
+    return Y
+
+
+def hyb_sddmm(h: Hybrid, G: torch.Tensor, B: torch.Tensor, S_ell: torch.Tensor | None = None,
+              S_ovf: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Dense to hybrid: (G . B^T) at A's nonzeros, in A's layout: (S_ell [rows, E], S_ovf [cap, cols])."""
+    R, N, ldg = _mat(G, name="G")
+    _, _, ldb = _mat(B, name="B")
+    S_ell = torch.empty((h.rows, h.E), dtype=torch.bfloat16, device=G.device) if S_ell is None else S_ell
+    S_ovf = torch.empty((max(h.cap, 1), h.cols), dtype=torch.bfloat16, device=G.device) if S_ovf is None else S_ovf
+    hc = h.c()
+    _check(lib.hyb_sddmm(C.byref(hc), G.data_ptr(), N, ldg, B.data_ptr(), ldb, S_ell.data_ptr(), S_ovf.data_ptr(),
+                         S_ovf.stride(0), _stream(stream)), "hyb_sddmm")
+    return S_ell, S_ovf

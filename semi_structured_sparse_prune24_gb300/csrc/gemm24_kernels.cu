@@ -69,6 +69,12 @@ struct SpmmParams {
   int b3d;  // B map is 3-D: {64 K, rows, K / 64}; one load brings both 64-K halves of a stage
   int nad;  // dense stages per tile after the sparse ones: A_l [rowsA, r] . B_l [rowsB, r]^T, 64 of r each
   int stall_stage;  // test only: if > 0, both CTAs of cluster 0 skip the loads of their stage number stall_stage - 1
+  // V:2:M sparse A (gathered B): A holds, per row block of vnm_V rows and group of vnm_group
+  // columns of the logical K, the values at 4 selected columns (condensed, 2:4 along them);
+  // vnm_cix [blocks, vnm_G] packs each group's 4 column offsets in one word (byte j =
+  // offset j). B is K-outer [vnm_K rows, rowsB columns]; stage rows are gathered by TMA.
+  const uint32_t* vnm_cix;
+  int vnm_group, vnm_V, vnm_G, vnm_K;
 };
 
 struct DwParams {
@@ -220,6 +226,17 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// Four rows y0..y3 of a 2-D map (box: 64 columns x 1 row), columns x..x+63, land as
+// four consecutive 128-byte rows at dst (the map's swizzle applies, as for a tile
+// load); the bytes complete on the pair leader's barrier.
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y0,
+                                                 int y1, int y2, int y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
 __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -251,7 +268,7 @@ enum SpmmEpi : int {
   kEpiFull = 1,   // any of: ReLU' gate, 2:4 activation prune, column sums (transposed output)
 };
 
-template <int BN, int STAGES, bool kTransOut, int kEpi>
+template <int BN, int STAGES, bool kTransOut, int kEpi, bool kGather = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmL,
@@ -263,7 +280,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   constexpr int kAccBufs = BN > 192 ? 1 : 2;
   static_assert(BN <= 256 && BN % 16 == 0, "tile width");
   static_assert(kAccBufs == 1 ? 256 + 8 * 4 * STAGES <= 512 : 4 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
-  constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, false);
+  // gathered B is staged MN-major: [K rows][N columns] in 64-column, 128B-swizzled atoms
+  constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, /*b_mn=*/kGather);
+  static_assert(!kGather || (!kTransOut && BN == 256), "gathered B: straight output, N = 256 tiles");
   constexpr uint32_t kIdescDense = idesc_bf16(2 * kBM, BN, /*sparse=*/false, false, false);
   const int nstages = p.nkb + p.nad;  // per tile: sparse stages, then dense ones
 
@@ -322,7 +341,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
-  if (warp == 0) {
+  if (warp == 0 && kGather) {
+    // ------------------------------------------------ TMA producer, gathered B (whole warp, both CTAs)
+    // Per stage (128 condensed K = 32 groups of 4 selected columns): lane 0 loads A and
+    // the metadata like the plain producer; lane l gathers group 32 kb + l's 4 rows of
+    // B (its columns of this CTA's half of the tile), one gather4 per 64 columns.
+    uint32_t it = 0, eit = 0;
+    bool ok = true;
+    for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+      int ta, tb;
+      tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
+      const uint32_t* cix = p.vnm_cix + static_cast<int64_t>((ta * 2 * kBM) / p.vnm_V) * p.vnm_G;
+      ta = 2 * ta + rank;
+      const int n0 = tb * BN + rank * (BN / 2);
+      // this lane's group offsets for the next kPf stages, loaded kPf stages ahead: when the
+      // gathers limit the pipeline the ring never fills, so a shorter distance would put an
+      // L2 round trip into every stage
+      constexpr int kPf = 4;
+      uint32_t c4r[kPf];
+#pragma unroll
+      for (int j = 0; j < kPf; ++j) c4r[j] = j < p.nkb ? __ldg(cix + 32 * j + lane) : 0u;
+      for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kPf) {
+#pragma unroll
+      for (int jj = 0; jj < kPf; ++jj) {
+        const int kb = kb0 + jj;
+        if (kb >= p.nkb) break;
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        const uint32_t c4 = c4r[jj];
+        int good = 1;
+        if (kb % kEStages == 0) {  // next metadata block
+          const int e = eit % kEBufs;
+          if (lane == 0) {
+            good = p24_wait(&eempty[e], ((eit / kEBufs) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+            if (good) {
+              mbar_arrive_expect_tx(&efull[e], L::kE);
+              tma_load_2d(smem + L::kOffE + e * L::kE, &tmE, &efull[e], (kb / kEStages) * 64, ta * kBM);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+          ++eit;
+        }
+        if (lane == 0) good = p24_wait(&empty[s], ph ^ 1, abort_flag, p.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        const uint32_t fullL = leader_addr(&full[s]);
+        if (lane == 0) {
+          if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
+          tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 64, ta * kBM);
+        }
+        const int g = kb * 32 + lane;  // every stage is full: the host requires 128 | condensed K
+        const int yb = g * p.vnm_group;
+        const int y0 = yb + static_cast<int>(c4 & 0xFFu), y1 = yb + static_cast<int>((c4 >> 8) & 0xFFu);
+        const int y2 = yb + static_cast<int>((c4 >> 16) & 0xFFu), y3 = yb + static_cast<int>(c4 >> 24);
+        c4r[jj] = (kb + kPf < p.nkb) ? __ldg(cix + g + 32 * kPf) : 0u;
+        uint8_t* bst = smem + L::kOffB + s * L::kB + lane * 512;
+#pragma unroll
+        for (int a = 0; a < BN / 128; ++a) tma_gather4_pair(bst + a * 16384, &tmB, fullL, n0 + a * 64, y0, y1, y2, y3);
+        __syncwarp();
+        ++it;
+      }
+      }
+    }
+    // Drain: the last issued loads must land before the CTA may exit.
+    if (lane == 0) {
+      const uint32_t n_drain = it < STAGES ? it : STAGES;
+      for (uint32_t i = 0; i < n_drain; ++i) {
+        const uint32_t j = it - 1 - i;
+        if (leader) p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
+      }
+      const uint32_t e_drain = eit < kEBufs ? eit : kEBufs;
+      for (uint32_t i = 0; i < e_drain; ++i) {
+        const uint32_t j = eit - 1 - i;
+        p24_wait_quiet(&efull[j % kEBufs], (j / kEBufs) & 1);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       uint32_t it = 0, eit = 0;
@@ -408,8 +501,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 const uint64_t adesc = smem_desc(a_base + j * 32, 16, 1024, kSwizzle128B);
+                // K-major B: 64-K halves of BN/2 rows; gathered (MN-major) B: 32 K rows per
+                // MMA in 64-column atoms of 128 rows (atom stride 16 KB, 8-row groups 1 KB)
                 const uint64_t bdesc =
-                    smem_desc(b_base + (j >> 1) * L::kBHalf + (j & 1) * 64, 16, 1024, kSwizzle128B);
+                    kGather ? smem_desc(b_base + j * 4096, 16384, 1024, kSwizzle128B)
+                            : smem_desc(b_base + (j >> 1) * L::kBHalf + (j & 1) * 64, 16, 1024, kSwizzle128B);
                 tc_mma_sp_pair(d_tmem, adesc, bdesc, tmem + meta_col<BN>(s, j), kIdesc, (kb | j) != 0);
               }
             } else {  // dense stage: 4 x K=16 of the low-rank product, into the same accumulator
@@ -994,11 +1090,11 @@ constexpr int kSpBNOverlap = 192;
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 6;
 
-template <int BN, bool kTrans, int kEpi>
+template <int BN, bool kTrans, int kEpi, bool kGather = false>
 cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const CUtensorMap& l,
                      const CUtensorMap& t, const SpmmParams& p, cudaStream_t s) {
   using L = SpmmSmem<BN, kSpStages>;
-  auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi>;
+  auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi, kGather>;
   const int smem = L::kBytes + 1024;
   static LaunchSetup setup;
   int clusters = 0;
@@ -1012,6 +1108,12 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
 }
 
 }  // namespace
+
+bool make_tensor_map_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, bf16 ? 2 : 1, base,
+                     inner, outer, row_bytes, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 
 cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out, int64_t ldo,
                         bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s) {
@@ -1104,6 +1206,42 @@ cudaError_t launch_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   return run_spmm<kSpBNWide, false, kEpiStore>(tl, tt, tl, tl, tt, p, s);
+}
+
+cudaError_t launch_vnm_spmm(const uint8_t* colidx, const p24_sparse& A, int V, int Mg, const void* B, int64_t N,
+                            int64_t ldb, const float* bias, bool relu, void* Y, int64_t ldy, int* status,
+                            cudaStream_t s) {
+  if (A.rows == 0 || N == 0) return cudaSuccess;
+  // the caller checked: V % 256 == 0, condensed K % 128 == 0, N % 256 == 0
+  const int64_t K = A.cols / 4 * Mg;  // logical reduction length (rows of B)
+  SpmmParams p{};
+  p.rowsA = static_cast<int>(A.rows);
+  p.rowsB = static_cast<int>(N);
+  p.K = static_cast<int>(A.cols);
+  p.tilesA = static_cast<int>((A.rows + 2 * kBM - 1) / (2 * kBM));
+  p.tilesB = static_cast<int>(N / kSpBNWide);
+  p.num_tiles = p.tilesA * p.tilesB;
+  p.group = std::min(p.tilesA, 16);
+  p.nkb = static_cast<int>(A.cols / 128);
+  p.out = static_cast<__nv_bfloat16*>(Y);
+  p.ldo = ldy;
+  p.bias = bias;
+  p.relu = relu ? 1 : 0;
+  p.status = status;
+  p.vnm_cix = reinterpret_cast<const uint32_t*>(colidx);
+  p.vnm_group = Mg;
+  p.vnm_V = V;
+  p.vnm_G = static_cast<int>(K / Mg);
+  p.vnm_K = static_cast<int>(K);
+  CUtensorMap ta, tb, te;
+  if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 64, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      // B [K, N]: one-row boxes of 64 columns, the gather4 form
+      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  return run_spmm<kSpBNWide, false, kEpiStore, true>(ta, tb, te, ta, tb, p, s);
 }
 
 namespace {

@@ -11,11 +11,6 @@
 #include "p24_internal.h"
 
 namespace p24 {
-// V:2:M prune + compress (prune24_kernels.cu): colidx [ceil(rows/V), cols/M, 4];
-// out = the condensed [rows, 4 cols/M] matrix in the 2:4 format.
-cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
-                                uint8_t* colidx, const p24_sparse& out, cudaStream_t s);
-
 namespace {
 
 // [0] P24_OK, or P24_ETIMEOUT after a bounded wait expired; [1] the CTA and [2] the
@@ -61,6 +56,8 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of ffn24_step, carved in this order (each region 256-byte aligned).
 struct StepLayout {
   p24_sparse up_fwd, up_bwdT, dn_fwd, dn_bwdT, hs;
+  uint8_t* colidx;  // V:N:M: H's kept column offsets [ceil(M/V), ffn/vM, 4]
+  void* wdmT;       // V:N:M: W_down on its 2:4 mask, transposed [ffn, d]
   // low-rank adapters: T_up, T_dn, U_dn, U_up [M, r]; Lt_up [r, ffn], Lt_dn [r, d], Rt_up [d, r], Rt_dn [ffn, r]
   void *T_up, *T_dn, *U_dn, *U_up, *Lt_up, *Lt_dn, *Rt_up, *Rt_dn;
   size_t off[16];
@@ -68,7 +65,7 @@ struct StepLayout {
 };
 
 void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r, char* base, StepLayout& L,
-                 void** wdm, void** dH, float** cs) {
+                 void** wdm, void** dH, float** cs, int64_t vV = 0, int64_t vM = 0) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char* p = base ? base + off : nullptr;
@@ -87,9 +84,16 @@ void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r, c
   sparse(L.up_bwdT, d, ffn);
   sparse(L.dn_fwd, d, ffn);
   sparse(L.dn_bwdT, ffn, d);
+  L.colidx = nullptr;
+  L.wdmT = nullptr;
   if (flags & P24_STEP_ACT24) {
     sparse(L.hs, M, ffn);
     *wdm = take(static_cast<size_t>(d * ffn * 2));
+  } else if ((flags & P24_STEP_VNM) && vV > 0 && vM > 0) {
+    sparse(L.hs, M, 4 * (ffn / vM));  // the condensed H
+    L.colidx = static_cast<uint8_t*>(take(static_cast<size_t>((M + vV - 1) / vV * (ffn / vM) * 4)));
+    L.wdmT = take(static_cast<size_t>(d * ffn * 2));
+    *wdm = nullptr;
   } else {
     std::memset(&L.hs, 0, sizeof(L.hs));
     *wdm = nullptr;
@@ -171,7 +175,7 @@ int prune24_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw
 }
 
 int vnm24_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int64_t V, int64_t M, uint8_t* colidx,
-                   const p24_sparse* out, void* stream) {
+                   const p24_sparse* out, void* A_masked, int64_t ldam, void* stream) {
   if (V < 1 || V > kMaxDim) return P24_EINVAL;
   if (M < 4 || M > 128 || M % 4 != 0 || 256 % M != 0) return P24_EINVAL;
   if (cols % M != 0) return P24_EINVAL;
@@ -179,8 +183,36 @@ int vnm24_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int64
   P24_TRY(check_sparse(out));
   if (out->rows != rows || out->cols != 4 * (cols / M)) return P24_EINVAL;
   if (rows > 0 && cols > 0 && !colidx) return P24_EINVAL;
+  if (A_masked) {
+    P24_TRY(check_dense(A_masked, rows, cols, ldam));
+    if (A_masked == A && ldam != lda) return P24_EINVAL;
+    if (V > 256 || cols % 8 != 0) return P24_EUNSUPPORTED;
+  }
   return cuda_status(launch_vnm_compress(A, rows, cols, lda, static_cast<int>(V), static_cast<int>(M), colidx, *out,
-                                         as_stream(stream)));
+                                         A_masked, ldam, as_stream(stream)));
+}
+
+int vnm24_spmm(const uint8_t* colidx, const p24_sparse* A, int64_t V, int64_t M, const void* B, int64_t N, int64_t ldb,
+               const float* bias, uint32_t flags, void* Y, int64_t ldy, void* stream) {
+  if (flags & ~(P24_EPI_BIAS | P24_EPI_RELU)) return P24_EINVAL;
+  if (V < 1 || V > kMaxDim) return P24_EINVAL;
+  if (M < 4 || M > 128 || M % 4 != 0 || 256 % M != 0) return P24_EINVAL;
+  P24_TRY(check_sparse(A));
+  const int64_t R = A->rows, Kc = A->cols;
+  const int64_t K = Kc / 4 * M;
+  if (K > kMaxDim || N < 0 || N > kMaxDim) return P24_EINVAL;
+  P24_TRY(check_dense(B, K, N, ldb));
+  P24_TRY(check_dense(Y, R, N, ldy));
+  if ((flags & P24_EPI_BIAS) && !bias) return P24_EINVAL;
+  if (R == 0 || N == 0) return P24_OK;
+  if (!colidx) return P24_EINVAL;
+  if (!aligned16(colidx)) return P24_EALIGN;
+  if (Kc == 0 || V % 256 != 0 || Kc % 128 != 0 || N % 256 != 0) return P24_EUNSUPPORTED;
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_vnm_spmm(colidx, *A, static_cast<int>(V), static_cast<int>(M), B, N, ldb,
+                                     (flags & P24_EPI_BIAS) ? bias : nullptr, (flags & P24_EPI_RELU) != 0, Y, ldy, st,
+                                     as_stream(stream)));
 }
 
 namespace {
@@ -380,6 +412,18 @@ size_t ffn24_workspace_size(int64_t M, int64_t d, int64_t ffn, uint32_t flags) {
   return ffn24_workspace_size_lowrank(M, d, ffn, flags, 0);
 }
 
+size_t ffn24_workspace_size_args(const p24_ffn_args* a) {
+  if (!a || a->M < 0 || a->d < 0 || a->ffn < 0 || a->r < 0) return 0;
+  const bool vnm = (a->flags & P24_STEP_VNM) != 0;
+  if (vnm && (a->vnm_V <= 0 || a->vnm_M < 4 || a->vnm_M % 4 != 0 || a->ffn % a->vnm_M != 0)) return 0;
+  StepLayout L;
+  void *wdm, *dH;
+  float* cs;
+  step_layout(a->M, a->d, a->ffn, a->flags, (a->flags & P24_STEP_ADAPTERS) ? a->r : 0, nullptr, L, &wdm, &dH, &cs,
+              vnm ? a->vnm_V : 0, vnm ? a->vnm_M : 0);
+  return L.total;
+}
+
 int ffn24_step(const p24_ffn_args* a, void* workspace, size_t ws_bytes, void* stream) {
   return ffn24_step_traced(a, workspace, ws_bytes, stream, nullptr, 0);
 }
@@ -390,10 +434,17 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
                       int n_events) {
   if (!a) return P24_EINVAL;
   if (n_events < 0 || (n_events > 0 && !events)) return P24_EINVAL;
-  if (a->flags & ~(P24_STEP_ACT24 | P24_STEP_KEEP_MASKS | P24_STEP_ADAPTERS)) return P24_EINVAL;
+  if (a->flags & ~(P24_STEP_ACT24 | P24_STEP_KEEP_MASKS | P24_STEP_ADAPTERS | P24_STEP_VNM)) return P24_EINVAL;
   const int64_t M = a->M, d = a->d, ffn = a->ffn;
   if (M < 0 || d <= 0 || ffn <= 0 || d % 8 != 0 || ffn % 8 != 0) return P24_EINVAL;
   const bool act24 = (a->flags & P24_STEP_ACT24) != 0;
+  const bool vnm = (a->flags & P24_STEP_VNM) != 0;
+  const int64_t vV = vnm ? a->vnm_V : 0, vM = vnm ? a->vnm_M : 0;
+  if (vnm) {
+    if (vM < 4 || vM > 128 || vM % 4 != 0 || 256 % vM != 0 || vV < 1) return P24_EINVAL;
+    if (act24 || (a->flags & P24_STEP_ADAPTERS)) return P24_EUNSUPPORTED;
+    if (vV != 256 || ffn % (32 * vM) != 0 || d % 256 != 0) return P24_EUNSUPPORTED;
+  }
   const bool keep = (a->flags & P24_STEP_KEEP_MASKS) != 0;
   // caller's compressed weights: required with fixed masks, optional otherwise
   const p24_sparse* cw[4] = {a->up_fwd, a->up_bwdT, a->down_fwd, a->down_bwdT};
@@ -443,7 +494,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   StepLayout L;
   void *wdm, *dHv;
   float* cs;
-  step_layout(M, d, ffn, a->flags, ad ? r : 0, static_cast<char*>(workspace), L, &wdm, &dHv, &cs);
+  step_layout(M, d, ffn, a->flags, ad ? r : 0, static_cast<char*>(workspace), L, &wdm, &dHv, &cs, vV, vM);
   if (ws_bytes < L.total) return P24_ENOSPACE;
   const cudaStream_t s = as_stream(stream);
   int* st = device_status_ptr();
@@ -461,6 +512,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   } while (0)
 
   // caller buffers replace the workspace's copies
+  const p24_sparse ws_dn_bwdT = L.dn_bwdT;
   if (a->up_fwd) L.up_fwd = *a->up_fwd;
   if (a->up_bwdT) L.up_bwdT = *a->up_bwdT;
   if (a->down_fwd) L.dn_fwd = *a->down_fwd;
@@ -478,9 +530,24 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
     }
   });
   P24_PHASE(1, {
-    if (!keep)
+    if (vnm) {
+      // W_down on its mask, transposed [ffn, d]: the gathered operand of the V:2:M down GEMM
+      // (a caller's W_down_masked, if any, is written by a plain compress beside it)
+      if (!keep) {
+        P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT, nullptr, 0, s,
+                                                 L.wdmT, d)));
+        // the caller's row-major W_down on its mask, if asked for (the forward prune again)
+        if (a->W_down_masked)
+          P24_TRY(cuda_status(launch_compress(a->W_down, d, ffn, ffn, L.dn_fwd, a->W_down_masked, ffn, s)));
+      } else {
+        // fixed masks: from the caller's compressed W_down; its double prune goes to the
+        // workspace's copy (the caller's buffers are read only)
+        P24_TRY(cuda_status(launch_transpose_repack(L.dn_fwd, ws_dn_bwdT, s, L.wdmT, d)));
+      }
+    } else if (!keep) {
       P24_TRY(cuda_status(launch_compress_both(a->W_down, d, ffn, ffn, L.dn_fwd, L.dn_bwdT,
                                                (act24 || a->W_down_masked) ? wdm : nullptr, ffn, s)));
+    }
     if (ad) {
       P24_TRY(cuda_status(launch_transpose_bf16(a->L_down, d, r, r, L.Lt_dn, d, s)));
       P24_TRY(cuda_status(launch_transpose_bf16(a->R_down, r, ffn, ffn, L.Rt_dn, r, s)));
@@ -510,6 +577,10 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
     if (ad) P24_TRY(cuda_status(launch_gemm_nt(a->X, M, d, a->R_up, r, d, d, L.T_up, r, st, s)));
     P24_TRY(cuda_status(launch_spmm(L.up_fwd, a->X, M, d, a->H, ffn, true, up, st, s)));
     if (act24) P24_TRY(cuda_status(launch_pad(L.hs, s)));
+    // V:N:M: prune H V:2:M along ffn, in place, and keep its condensed form for the down GEMM
+    if (vnm)
+      P24_TRY(cuda_status(launch_vnm_compress(a->H, M, ffn, ffn, static_cast<int>(vV), static_cast<int>(vM),
+                                              L.colidx, L.hs, a->H, ffn, s)));
   });
   // 3. Y = H W_down^T + b_down
   EpiArgs dn;
@@ -522,6 +593,9 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   P24_PHASE(3, {
     if (ad) P24_TRY(cuda_status(launch_gemm_nt(a->H, M, ffn, a->R_down, r, ffn, ffn, L.T_dn, r, st, s)));
     if (act24) P24_TRY(cuda_status(launch_spmm(L.hs, wdm, d, ffn, a->Y, d, false, dn, st, s)));
+    else if (vnm)
+      P24_TRY(cuda_status(launch_vnm_spmm(L.colidx, L.hs, static_cast<int>(vV), static_cast<int>(vM), L.wdmT, d, d,
+                                          a->b_down, false, a->Y, d, st, s)));
     else P24_TRY(cuda_status(launch_spmm(L.dn_fwd, a->H, M, ffn, a->Y, d, true, dn, st, s)));
   });
   // 4. dH = (dY W_down_bwd) * [H > 0], with db_up = column sums of dH fused into its epilogue
@@ -588,6 +662,56 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   return P24_OK;
 }
 
+namespace {
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_hybrid(const p24_hybrid* h) {
+  if (!h) return P24_EINVAL;
+  if (h->rows < 0 || h->rows > kMaxDim || h->cols < 0 || h->cols > 65536 || h->E < 1 || h->E > kMaxDim ||
+      h->cap < 0 || h->cap > kMaxDim)
+    return P24_EINVAL;
+  if (h->cols % 8 != 0) return P24_EINVAL;
+  if (h->rows == 0) return P24_OK;
+  if (!h->nnz || !h->ell_cols || !h->ell_vals || !h->slot || !h->n_ovf) return P24_EINVAL;
+  if (h->cap > 0 && (!h->ovf_rows || !h->ovf)) return P24_EINVAL;
+  if (!aligned4(h->nnz) || !aligned4(h->slot) || !aligned4(h->n_ovf) || (h->cap > 0 && !aligned4(h->ovf_rows)))
+    return P24_EALIGN;
+  if (!aligned16(h->ell_cols) || !aligned16(h->ell_vals)) return P24_EALIGN;
+  if (h->cap > 0) P24_TRY(check_dense(h->ovf, h->cap, h->cols, h->ldo));
+  return P24_OK;
+}
+}  // namespace
+
+int hyb_compress(const void* A, int64_t lda, const p24_hybrid* h, void* stream) {
+  P24_TRY(check_hybrid(h));
+  P24_TRY(check_dense(A, h->rows, h->cols, lda));
+  if (h->rows == 0) return P24_OK;
+  int* st = device_status_ptr();
+  if (!st) return P24_ECUDA;
+  return cuda_status(launch_hyb_compress(A, lda, *h, st, as_stream(stream)));
+}
+
+int hyb_spmm(const p24_hybrid* h, const void* B, int64_t N, int64_t ldb, void* Y, int64_t ldy, void* stream) {
+  P24_TRY(check_hybrid(h));
+  if (N < 0 || N > kMaxDim || N % 8 != 0) return P24_EINVAL;
+  P24_TRY(check_dense(B, h->cols, N, ldb));
+  P24_TRY(check_dense(Y, h->rows, N, ldy));
+  if (h->rows == 0 || N == 0) return P24_OK;
+  return cuda_status(launch_hyb_spmm(*h, B, N, ldb, Y, ldy, as_stream(stream)));
+}
+
+int hyb_sddmm(const p24_hybrid* h, const void* G, int64_t N, int64_t ldg, const void* B, int64_t ldb, void* S_ell,
+              void* S_ovf, int64_t lds, void* stream) {
+  P24_TRY(check_hybrid(h));
+  if (N < 0 || N > 32768 || N % 8 != 0) return P24_EINVAL;  // G's row is staged in shared memory
+  P24_TRY(check_dense(G, h->rows, N, ldg));
+  P24_TRY(check_dense(B, h->cols, N, ldb));
+  if (h->rows > 0 && (!S_ell || !aligned16(S_ell))) return S_ell ? P24_EALIGN : P24_EINVAL;
+  if (h->cap > 0) P24_TRY(check_dense(S_ovf, h->cap, h->cols, lds));
+  if (h->rows == 0) return P24_OK;
+  return cuda_status(launch_hyb_sddmm(*h, G, N, ldg, B, ldb, S_ell, S_ovf, lds, as_stream(stream)));
+}
+
 int p24_selftest_timeout(int64_t limit_ns, void* stream) {
   if (limit_ns <= 0 || limit_ns > 10000000000LL) return P24_EINVAL;
   int* st = device_status_ptr();
@@ -617,6 +741,7 @@ const char* p24_strerror(int code) {
     case P24_ETIMEOUT: return "a kernel's bounded wait expired";
     case P24_EUNSUPPORTED: return "unsupported device or shape";
     case P24_ENOSPACE: return "workspace too small";
+    case P24_ECAPACITY: return "a data-dependent output exceeded its capacity";
     default: return "unknown status";
   }
 }

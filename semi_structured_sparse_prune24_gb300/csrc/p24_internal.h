@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "prune24.h"
@@ -12,9 +13,13 @@ namespace p24 {
 // ---- pruning / packing (prune24_kernels.cu) ----
 cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& out,
                             void* W_masked, int64_t ldwm, cudaStream_t s);
+// W_masked_T (optional, not together with W_masked): the forward-masked W transposed, [cols, ldwmT].
 cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& fwd,
-                                 const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s);
-cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s);
+                                 const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s,
+                                 void* W_masked_T = nullptr, int64_t ldwmT = 0);
+// W_masked_T (optional): the forward-masked matrix transposed, [fwd.cols, ldwmT].
+cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s,
+                                    void* W_masked_T = nullptr, int64_t ldwmT = 0);
 cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s);
 int64_t colsum_slabs(int64_t M);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
@@ -47,6 +52,15 @@ struct EpiArgs {
 cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out,
                         int64_t ldo, bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s);
 
+// Y [R, N] = act(A . B + bias) with A V:2:M-sparse (colidx [ceil(R/V), K/Mg, 4] and the
+// condensed 2:4 descriptor, cols = 4 K / Mg) and B dense K-outer [K, ldb]. Requires
+// V % 256 == 0, A.cols % 128 == 0 and N % 256 == 0 (checked by the caller).
+cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
+                                uint8_t* colidx, const p24_sparse& out, void* A_masked, int64_t ldam, cudaStream_t s);
+cudaError_t launch_vnm_spmm(const uint8_t* colidx, const p24_sparse& A, int V, int Mg, const void* B, int64_t N,
+                            int64_t ldb, const float* bias, bool relu, void* Y, int64_t ldy, int* status,
+                            cudaStream_t s);
+
 // dW[n, k] = sum_m dY[m, n] * X[m, k] on mask(meta) (both operands MN-major).
 // C [M, N] = A [M, K] . B [N, K]^T, bf16 in and out, fp32 accumulation (K-major operands).
 cudaError_t launch_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B, int64_t N, int64_t ldb, int64_t K,
@@ -74,6 +88,18 @@ cudaError_t launch_masked_dw_extra(const void* dY, int64_t lddy, const void* X, 
 cudaError_t launch_masked_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int64_t M, int64_t N,
                              int64_t K, const uint8_t* meta, int64_t ldm, void* dW, int64_t lddw, int* status,
                              cudaStream_t s);
+
+// ---- hybrid ELL + dense-overflow activations (hyb_kernels.cu)
+cudaError_t launch_hyb_compress(const void* A, int64_t lda, const p24_hybrid& h, int* status, cudaStream_t s);
+cudaError_t launch_hyb_spmm(const p24_hybrid& h, const void* B, int64_t N, int64_t ldb, void* Y, int64_t ldy,
+                            cudaStream_t s);
+cudaError_t launch_hyb_sddmm(const p24_hybrid& h, const void* G, int64_t N, int64_t ldg, const void* B, int64_t ldb,
+                             void* S_ell, void* S_ovf, int64_t lds, cudaStream_t s);
+
+// A 2-D tensor map (no swizzle) over a row-major matrix, for the HBM-bound kernels'
+// TMA staging: `inner` columns of `outer` rows, boxes of box_inner x box_outer.
+bool make_tensor_map_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
 int* device_status_ptr();  // the status word of the current device
 

@@ -238,6 +238,219 @@ __global__ void __launch_bounds__(256) vnm_compress_kernel(const uint16_t* __res
   }
 }
 
+// The same prune with the CTA's block (V <= 256 rows x CW columns) staged in shared
+// memory: one coalesced pass of 16-byte loads brings the block on chip, the column
+// norms (same fp32 order: rows of the block top to bottom), the selection and the
+// row prunes then read shared memory, and the optional dense masked output is
+// written back from it with 16-byte stores. The whole block is read before anything
+// is written, so the masked output may overwrite A in place.
+// CW = 64 for M <= 32, else 2 M (CW / M is even, so whole metadata bytes fall in one CTA).
+__global__ void __launch_bounds__(256) vnm_compress_staged_kernel(
+    const uint16_t* A, int64_t rows, int64_t cols, int64_t lda, int V, int M, int CW,
+    uint8_t* __restrict__ colidx, uint16_t* __restrict__ vals, int64_t ldv, uint8_t* __restrict__ meta, int64_t ldm,
+    uint16_t* Am, int64_t ldam) {
+  extern __shared__ __align__(16) uint16_t tile[];  // [V][CW]
+  __shared__ uint32_t key[256];
+  __shared__ uint8_t kept[256];
+  __shared__ uint8_t offs[256];  // [group in chunk][slot 0..3]
+  const int t = threadIdx.x;
+  const int64_t G = cols / M;
+  const int64_t nb = (rows + V - 1) / V;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CW;
+  const int ncol = static_cast<int>(min(static_cast<int64_t>(CW), cols - c0));  // a multiple of M and of 8
+  const int cpr = ncol / 8;                       // 16-byte chunks per row
+  const int j = t % M, gstart = t - j;            // column within its group, group's first column
+  const int gpc = ncol / M;                       // groups in this chunk (odd only in a row's last chunk)
+  for (int64_t b = blockIdx.y; b < nb; b += gridDim.y) {
+    const int64_t r0 = b * V;
+    const int nr = static_cast<int>(min(rows - r0, static_cast<int64_t>(V)));
+    // 1. stage the block
+    const int nchunks = nr * cpr;
+    for (int i0 = t; i0 < nchunks; i0 += 4 * 256) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 256;
+        if (i < nchunks) v[u] = ld_stream_v4(A + (r0 + i / cpr) * lda + c0 + (i % cpr) * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 256;
+        if (i < nchunks) *reinterpret_cast<uint4*>(tile + (i / cpr) * CW + (i % cpr) * 8) = v[u];
+      }
+    }
+    __syncthreads();
+    // 2. column norm over the block, rows in order
+    if (t < ncol) {
+      float sum = 0.f;
+      for (int r = 0; r < nr; ++r) sum += __uint_as_float(static_cast<uint32_t>(tile[r * CW + t] & 0x7FFFu) << 16);
+      key[t] = (sum != sum) ? 0x7FC00000u : __float_as_uint(sum);
+    }
+    __syncthreads();
+    // 3. selection and slot
+    if (t < ncol) {
+      const uint32_t k = key[t];
+      int beat = 0;
+      for (int q = 0; q < M; ++q) {
+        const uint32_t kq = key[gstart + q];
+        beat += (kq > k || (kq == k && q < j)) ? 1 : 0;
+      }
+      kept[t] = beat < 4 ? 1 : 0;
+    }
+    __syncthreads();
+    if (t < ncol && kept[t]) {
+      int slot = 0;
+      for (int q = 0; q < j; ++q) slot += kept[gstart + q];
+      offs[(t / M) * 4 + slot] = static_cast<uint8_t>(j);
+      colidx[(b * G + (c0 + t) / M) * 4 + slot] = static_cast<uint8_t>(j);
+    }
+    __syncthreads();
+    // 4. rows x pairs of groups: 2:4 among the 4 kept columns; the tile keeps only the
+    //    2 survivors of each group (for the masked output)
+    const int pairs = (gpc + 1) / 2;
+    const int64_t g_first = c0 / M;                 // even: CW / M is even
+    for (int w = t; w < nr * pairs; w += 256) {
+      const int r = w / pairs;
+      const int pl = w % pairs;
+      uint32_t nib[2] = {0x4u, 0x4u};               // a missing last group keeps the padding nibble
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int gl = 2 * pl + h;
+        if (gl >= gpc) break;
+        uint16_t* a = tile + r * CW + gl * M;
+        const uint8_t* o = offs + gl * 4;
+        const uint32_t lo = static_cast<uint32_t>(a[o[0]]) | (static_cast<uint32_t>(a[o[1]]) << 16);
+        const uint32_t hi = static_cast<uint32_t>(a[o[2]]) | (static_cast<uint32_t>(a[o[3]]) << 16);
+        nib[h] = pick2_nibble(lo, hi);
+        *reinterpret_cast<uint32_t*>(vals + (r0 + r) * ldv + 2 * (g_first + gl)) = kept_pair(lo, hi, nib[h]);
+        if (Am) {
+          const int k0 = o[nib[h] & 3u], k1 = o[nib[h] >> 2];
+          for (int q = 0; q < M; ++q)
+            if (q != k0 && q != k1) a[q] = 0;
+        }
+      }
+      meta[(r0 + r) * ldm + (g_first + 2 * pl) / 2] = static_cast<uint8_t>(nib[0] | (nib[1] << 4));
+    }
+    if (Am) {
+      __syncthreads();
+      for (int i = t; i < nchunks; i += 256)
+        *reinterpret_cast<uint4*>(Am + (r0 + i / cpr) * ldam + c0 + (i % cpr) * 8) =
+            *reinterpret_cast<const uint4*>(tile + (i / cpr) * CW + (i % cpr) * 8);
+    }
+    __syncthreads();
+  }
+}
+
+// The same prune as a persistent kernel: work item = (row block, CW-column chunk);
+// each item's V x CW tile is brought into shared memory by one TMA box while the
+// previous item is processed (two buffers), so the HBM stream overlaps the serial
+// fp32 column sums. Rows past the matrix arrive as zeros and add nothing to a sum.
+// After the prune pass has zeroed the dropped entries in shared memory, the tile is
+// the dense masked output and is written back with 16-byte stores.
+__global__ void __launch_bounds__(256) vnm_compress_tma_kernel(
+    const __grid_constant__ CUtensorMap tmA, int64_t rows, int64_t cols, int V, int M, int CW, int64_t n_items,
+    int64_t nbx, uint8_t* __restrict__ colidx, uint16_t* __restrict__ vals, int64_t ldv,
+    uint8_t* __restrict__ meta, int64_t ldm, uint16_t* Am, int64_t ldam, int* status) {
+  extern __shared__ __align__(128) uint16_t tiles[];  // 2 x [V][CW]
+  __shared__ uint32_t key[256];
+  __shared__ uint8_t kept[256];
+  __shared__ uint8_t offs[256];
+  __shared__ __align__(8) uint64_t full[2];
+  const int t = threadIdx.x;
+  const int64_t G = cols / M;
+  const int j = t % M, gstart = t - j;
+  const int tile_elems = V * CW;
+  if (t == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int64_t item = blockIdx.x;
+  if (t == 0 && item < n_items) {
+    mbar_arrive_expect_tx(&full[0], static_cast<uint32_t>(tile_elems * 2));
+    tma_load_2d(tiles, &tmA, &full[0], static_cast<int>((item % nbx) * CW), static_cast<int>((item / nbx) * V));
+  }
+  for (int i = 0; item < n_items; ++i, item += gridDim.x) {
+    const int buf = i & 1;
+    const int64_t next = item + gridDim.x;
+    if (t == 0 && next < n_items) {
+      // the other buffer was last read and written by this CTA's threads (generic
+      // proxy) before the barrier that ended the previous item
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&full[buf ^ 1], static_cast<uint32_t>(tile_elems * 2));
+      tma_load_2d(tiles + (buf ^ 1) * tile_elems, &tmA, &full[buf ^ 1], static_cast<int>((next % nbx) * CW),
+                  static_cast<int>((next / nbx) * V));
+    }
+    if (!p24_wait_for(&full[buf], (i >> 1) & 1, P24_WAIT_NS, status)) return;
+    uint16_t* tile = tiles + buf * tile_elems;
+    const int64_t b = item / nbx;
+    const int64_t c0 = (item % nbx) * CW;
+    const int64_t r0 = b * V;
+    const int nr = static_cast<int>(min(rows - r0, static_cast<int64_t>(V)));
+    const int ncol = static_cast<int>(min(static_cast<int64_t>(CW), cols - c0));
+    const int gpc = ncol / M;
+    // 1. column norm over the block, rows in order
+    if (t < ncol) {
+      float sum = 0.f;
+      for (int r = 0; r < nr; ++r) sum += __uint_as_float(static_cast<uint32_t>(tile[r * CW + t] & 0x7FFFu) << 16);
+      key[t] = (sum != sum) ? 0x7FC00000u : __float_as_uint(sum);
+    }
+    __syncthreads();
+    // 2. selection and slot
+    if (t < ncol) {
+      const uint32_t k = key[t];
+      int beat = 0;
+      for (int q = 0; q < M; ++q) {
+        const uint32_t kq = key[gstart + q];
+        beat += (kq > k || (kq == k && q < j)) ? 1 : 0;
+      }
+      kept[t] = beat < 4 ? 1 : 0;
+    }
+    __syncthreads();
+    if (t < ncol && kept[t]) {
+      int slot = 0;
+      for (int q = 0; q < j; ++q) slot += kept[gstart + q];
+      offs[(t / M) * 4 + slot] = static_cast<uint8_t>(j);
+      colidx[(b * G + (c0 + t) / M) * 4 + slot] = static_cast<uint8_t>(j);
+    }
+    __syncthreads();
+    // 3. rows x pairs of groups
+    const int pairs = (gpc + 1) / 2;
+    const int64_t g_first = c0 / M;
+    for (int w = t; w < nr * pairs; w += 256) {
+      const int r = w / pairs;
+      const int pl = w % pairs;
+      uint32_t nib[2] = {0x4u, 0x4u};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int gl = 2 * pl + h;
+        if (gl >= gpc) break;
+        uint16_t* a = tile + r * CW + gl * M;
+        const uint8_t* o = offs + gl * 4;
+        const uint32_t lo = static_cast<uint32_t>(a[o[0]]) | (static_cast<uint32_t>(a[o[1]]) << 16);
+        const uint32_t hi = static_cast<uint32_t>(a[o[2]]) | (static_cast<uint32_t>(a[o[3]]) << 16);
+        nib[h] = pick2_nibble(lo, hi);
+        *reinterpret_cast<uint32_t*>(vals + (r0 + r) * ldv + 2 * (g_first + gl)) = kept_pair(lo, hi, nib[h]);
+        if (Am) {
+          const int k0 = o[nib[h] & 3u], k1 = o[nib[h] >> 2];
+          for (int q = 0; q < M; ++q)
+            if (q != k0 && q != k1) a[q] = 0;
+        }
+      }
+      meta[(r0 + r) * ldm + (g_first + 2 * pl) / 2] = static_cast<uint8_t>(nib[0] | (nib[1] << 4));
+    }
+    if (Am) {
+      __syncthreads();
+      const int cpr = ncol / 8;
+      for (int q = t; q < nr * cpr; q += 256)
+        *reinterpret_cast<uint4*>(Am + (r0 + q / cpr) * ldam + c0 + (q % cpr) * 8) =
+            *reinterpret_cast<const uint4*>(tile + (q / cpr) * CW + (q % cpr) * 8);
+    }
+    __syncthreads();
+  }
+}
+
 // ---------------------------------------------------------------- double prune
 constexpr int kDpRows = 128, kDpCols = 128, kDpChunks = kDpCols / 8;
 
@@ -255,13 +468,13 @@ struct DpArgs {
   int64_t ldtv;
   uint8_t* tm;
   int64_t ldtm;
-  uint16_t* Wm;             // optional dense forward-masked copy
-  int64_t ldwm;
+  uint16_t* Wm;             // optional dense forward-masked copy: [rows, ldwm], or with
+  int64_t ldwm;             // kMaskedT its transpose [cols, ldwm]
 };
 
 // One 128 x 128 tile. kEdge: the tile crosses the last row or column, so every
 // access is checked; interior tiles (all but a thin border) skip the checks.
-template <bool kFromDense, bool kMasked, bool kEdge>
+template <bool kFromDense, bool kMasked, bool kEdge, bool kMaskedT>
 __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t col0, uint4* tile,
                                         const uint2* ptab) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -364,6 +577,8 @@ __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t c
       if (active) {
         *reinterpret_cast<uint32_t*>(tvp + j * p.ldtv) = pair;
         if ((lane & 1) == 0) tmp[j * p.ldtm] = static_cast<uint8_t>(nib | ((next_in ? nib_next : 0x4u) << 4));
+        // the forward-masked quad of column j, transposed: 4 consecutive values of a W^T row
+        if (kMaskedT) *reinterpret_cast<uint2*>(p.Wm + (cbase + j) * p.ldwm + 4 * hq) = make_uint2(lo, hi);
       }
     }
   }
@@ -384,7 +599,7 @@ __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t c
 // Interior tiles (whole 128 x 128 blocks) run without bounds checks, four CTAs
 // per SM; the border tiles of a ragged matrix (the last partial block column, then
 // the last partial block row) run checked in a second, small launch.
-template <bool kFromDense, bool kMasked>
+template <bool kFromDense, bool kMasked, bool kMaskedT>
 __global__ void __launch_bounds__(256, 4) double_prune_interior_kernel(const DpArgs p, int64_t rows_full) {
   __shared__ uint4 tile[kDpRows * kDpChunks];
   __shared__ uint2 ptab[16];
@@ -393,10 +608,10 @@ __global__ void __launch_bounds__(256, 4) double_prune_interior_kernel(const DpA
   const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kDpCols;
   for (int64_t row0 = static_cast<int64_t>(blockIdx.y) * kDpRows; row0 < rows_full;
        row0 += static_cast<int64_t>(gridDim.y) * kDpRows)
-    dp_tile<kFromDense, kMasked, false>(p, row0, col0, tile, ptab);
+    dp_tile<kFromDense, kMasked, false, kMaskedT>(p, row0, col0, tile, ptab);
 }
 
-template <bool kFromDense, bool kMasked>
+template <bool kFromDense, bool kMasked, bool kMaskedT>
 __global__ void __launch_bounds__(256, 2) double_prune_border_kernel(const DpArgs p, int64_t n_col_part,
                                                                     int64_t full_bx, int64_t full_by) {
   __shared__ uint4 tile[kDpRows * kDpChunks];
@@ -406,24 +621,24 @@ __global__ void __launch_bounds__(256, 2) double_prune_border_kernel(const DpArg
   const int64_t t = blockIdx.x;
   const int64_t bx = t < n_col_part ? full_bx : t - n_col_part;
   const int64_t by = t < n_col_part ? t : full_by;
-  dp_tile<kFromDense, kMasked, true>(p, by * kDpRows, bx * kDpCols, tile, ptab);
+  dp_tile<kFromDense, kMasked, true, kMaskedT>(p, by * kDpRows, bx * kDpCols, tile, ptab);
 }
 
 inline unsigned grid_y(int64_t n) { return static_cast<unsigned>(n < 65535 ? (n < 1 ? 1 : n) : 65535); }
 
-template <bool kFromDense, bool kMasked>
+template <bool kFromDense, bool kMasked, bool kMaskedT = false>
 cudaError_t launch_double_prune(const DpArgs& a, cudaStream_t s) {
   const int64_t full_bx = a.cols / kDpCols, full_by = a.rows / kDpRows;
   const int64_t nby = (a.rows + kDpRows - 1) / kDpRows;
   if (full_bx > 0 && full_by > 0) {
     dim3 grid(static_cast<unsigned>(full_bx), grid_y(full_by));
-    double_prune_interior_kernel<kFromDense, kMasked><<<grid, 256, 0, s>>>(a, full_by * kDpRows);
+    double_prune_interior_kernel<kFromDense, kMasked, kMaskedT><<<grid, 256, 0, s>>>(a, full_by * kDpRows);
     count_launch();
   }
   const int64_t n_col_part = (a.cols % kDpCols) ? nby : 0;       // last block column, every block row
   const int64_t n_row_part = (a.rows % kDpRows) ? full_bx : 0;   // last block row, full block columns
   if (n_col_part + n_row_part > 0) {
-    double_prune_border_kernel<kFromDense, kMasked>
+    double_prune_border_kernel<kFromDense, kMasked, kMaskedT>
         <<<static_cast<unsigned>(n_col_part + n_row_part), 256, 0, s>>>(a, n_col_part, full_bx, full_by);
     count_launch();
   }
@@ -585,22 +800,87 @@ cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t l
 }
 
 cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& fwd,
-                                 const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s) {
+                                 const p24_sparse& bwdT, void* W_masked, int64_t ldwm, cudaStream_t s,
+                                 void* W_masked_T, int64_t ldwmT) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const auto* w = static_cast<const uint16_t*>(W);
+  // one dense masked copy at most: row-major (W_masked) or transposed (W_masked_T)
+  if (W_masked && W_masked_T) return cudaErrorInvalidValue;
   const DpArgs a{w,       ldw,  nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm,
                  rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm,
-                 static_cast<uint16_t*>(W_masked), ldwm};
-  cudaError_t e = W_masked ? launch_double_prune<true, true>(a, s) : launch_double_prune<true, false>(a, s);
+                 static_cast<uint16_t*>(W_masked_T ? W_masked_T : W_masked), W_masked_T ? ldwmT : ldwm};
+  cudaError_t e = W_masked_T ? launch_double_prune<true, false, true>(a, s)
+                             : (W_masked ? launch_double_prune<true, true>(a, s) : launch_double_prune<true, false>(a, s));
   if (e != cudaSuccess) return e;
   if ((e = launch_pad(fwd, s)) != cudaSuccess) return e;
   return launch_pad(bwdT, s);
 }
 
 cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64_t lda, int V, int M,
-                                uint8_t* colidx, const p24_sparse& out, cudaStream_t s) {
+                                uint8_t* colidx, const p24_sparse& out, void* A_masked, int64_t ldam, cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const int64_t nb = (rows + V - 1) / V;
+  if (V <= 256 && cols % 8 == 0 && 2 * V * (M <= 32 ? 64 : 2 * M) * 2 <= 128 * 1024) {
+    // persistent, TMA double-buffered: the narrowest chunk that still holds whole
+    // metadata bytes (two groups), two buffers of V x CW
+    const int CW = M <= 32 ? 64 : 2 * M;
+    const int smem = 2 * V * CW * 2;
+    CUtensorMap tm;
+    if (!make_tensor_map_2d(&tm, true, A, cols, rows, lda * 2, CW, V)) return cudaErrorInvalidValue;
+    int* status = device_status_ptr();
+    if (!status) return cudaErrorInvalidDevice;
+    static std::once_flag once_t[64];
+    static cudaError_t attr_t[64];
+    static int per_sm[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once_t[dev], [&] {
+      attr_t[dev] = cudaFuncSetAttribute(vnm_compress_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         128 * 1024);
+      int sms = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      per_sm[dev] = sms > 0 ? sms : 1;
+    });
+    if (attr_t[dev] != cudaSuccess) return attr_t[dev];
+    const int64_t nbx = (cols + CW - 1) / CW;
+    const int64_t n_items = nb * nbx;
+    const int64_t ctas_per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (200 * 1024) / (smem + 2048)));
+    const int64_t grid = std::min<int64_t>(n_items, per_sm[dev] * ctas_per_sm);
+    vnm_compress_tma_kernel<<<static_cast<unsigned>(grid), 256, smem, s>>>(
+        tm, rows, cols, V, M, CW, n_items, nbx, colidx, static_cast<uint16_t*>(out.vals), out.ldv, out.meta, out.ldm,
+        static_cast<uint16_t*>(A_masked), ldam, status);
+    count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pad(out, s);
+  }
+  if (V <= 256 && cols % 8 == 0) {
+    // staged: the block in shared memory (the widest groups, M = 128 with V > 128)
+    const int CW = M <= 32 ? 64 : 2 * M;
+    const int smem = V * CW * 2;
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [&] {
+      attr_err[dev] = cudaFuncSetAttribute(vnm_compress_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           256 * 256 * 2);
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    dim3 grid(static_cast<unsigned>((cols + CW - 1) / CW), grid_y(nb));
+    vnm_compress_staged_kernel<<<grid, 256, smem, s>>>(
+        static_cast<const uint16_t*>(A), rows, cols, lda, V, M, CW, colidx, static_cast<uint16_t*>(out.vals),
+        out.ldv, out.meta, out.ldm, static_cast<uint16_t*>(A_masked), ldam);
+    count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pad(out, s);
+  }
+  if (A_masked) return cudaErrorInvalidValue;  // the masked output needs the staged kernel (V <= 256)
   dim3 grid(static_cast<unsigned>((cols + kVnmCols - 1) / kVnmCols), grid_y(nb));
   vnm_compress_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(A), rows, cols, lda, V, M, colidx,
                                             static_cast<uint16_t*>(out.vals), out.ldv, out.meta, out.ldm);
@@ -610,12 +890,14 @@ cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64
   return launch_pad(out, s);
 }
 
-cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s) {
+cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwdT, cudaStream_t s, void* W_masked_T,
+                                    int64_t ldwmT) {
   const int64_t rows = fwd.rows, cols = fwd.cols;
   if (rows == 0 || cols == 0) return cudaSuccess;
   const DpArgs a{nullptr, 0,    static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm,
-                 rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm, nullptr, 0};
-  const cudaError_t e = launch_double_prune<false, false>(a, s);
+                 rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm,
+                 static_cast<uint16_t*>(W_masked_T), ldwmT};
+  const cudaError_t e = W_masked_T ? launch_double_prune<false, false, true>(a, s) : launch_double_prune<false, false>(a, s);
   if (e != cudaSuccess) return e;
   return launch_pad(bwdT, s);
 }

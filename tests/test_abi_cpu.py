@@ -153,10 +153,55 @@ def test_host_validation_of_vnm24_compress(native):
     EINVAL, EALIGN = native.P24_EINVAL, native.P24_EALIGN
     fake = 0x10000  # never dereferenced: every call below fails validation first
     out = _sp(fake, fake, 8, 16, 8, 16, native)          # condensed [8, 4*32/8 = 16]
-    assert L.vnm24_compress(fake, 8, 32, 32, 4, 12, fake, C.byref(out), None) == EINVAL   # M not dividing 256
-    assert L.vnm24_compress(fake, 8, 32, 32, 4, 256, fake, C.byref(out), None) == EINVAL  # M above 128
-    assert L.vnm24_compress(fake, 8, 36, 40, 4, 8, fake, C.byref(out), None) == EINVAL    # cols % M
-    assert L.vnm24_compress(fake, 8, 32, 32, 0, 8, fake, C.byref(out), None) == EINVAL    # V < 1
-    assert L.vnm24_compress(fake, 8, 32, 36, 4, 8, fake, C.byref(out), None) == EALIGN    # lda % 8
-    assert L.vnm24_compress(fake, 8, 32, 32, 4, 16, fake, C.byref(out), None) == EINVAL   # out is not [8, 8]
-    assert L.vnm24_compress(fake, 8, 32, 32, 4, 8, None, C.byref(out), None) == EINVAL    # no colidx
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 12, fake, C.byref(out), None, 0, None) == EINVAL   # M not dividing 256
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 256, fake, C.byref(out), None, 0, None) == EINVAL  # M above 128
+    assert L.vnm24_compress(fake, 8, 36, 40, 4, 8, fake, C.byref(out), None, 0, None) == EINVAL    # cols % M
+    assert L.vnm24_compress(fake, 8, 32, 32, 0, 8, fake, C.byref(out), None, 0, None) == EINVAL    # V < 1
+    assert L.vnm24_compress(fake, 8, 32, 36, 4, 8, fake, C.byref(out), None, 0, None) == EALIGN    # lda % 8
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 16, fake, C.byref(out), None, 0, None) == EINVAL   # out is not [8, 8]
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 8, None, C.byref(out), None, 0, None) == EINVAL    # no colidx
+
+
+def test_host_validation_of_vnm24_compress_masked_and_spmm(native):
+    L = native.lib
+    EINVAL, EALIGN, EUNS = native.P24_EINVAL, native.P24_EALIGN, native.P24_EUNSUPPORTED
+    fake = 0x10000  # never dereferenced: every call below fails validation first
+    out = _sp(fake, fake, 8, 16, 8, 16, native)
+    # masked output: in place needs the same stride; V above 256 is not supported with it
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 8, fake, C.byref(out), fake, 40, None) == EINVAL
+    assert L.vnm24_compress(fake, 8, 32, 32, 300, 8, fake, C.byref(out), fake + 0x1000, 32, None) == EUNS
+    assert L.vnm24_compress(fake, 8, 32, 32, 4, 8, fake, C.byref(out), fake + 8, 32, None) == EALIGN
+    # vnm24_spmm: A condensed [512, 256] from K = 512 (M = 8); B [512, 256]
+    a = _sp(fake, fake, 512, 256, 128, 32, native)
+    assert L.vnm24_spmm(fake, C.byref(a), 256, 8, fake, 256, 256, None, 0x8, fake, 256, None) == EINVAL  # flag
+    assert L.vnm24_spmm(fake, C.byref(a), 256, 12, fake, 256, 256, None, 0, fake, 256, None) == EINVAL   # M
+    assert L.vnm24_spmm(fake, C.byref(a), 0, 8, fake, 256, 256, None, 0, fake, 256, None) == EINVAL      # V
+    assert L.vnm24_spmm(fake, C.byref(a), 256, 8, fake, 256, 200, None, 0, fake, 256, None) == EINVAL    # ldb < N
+    assert L.vnm24_spmm(fake, C.byref(a), 256, 8, fake, 256, 256, None, 1, fake, 256, None) == EINVAL    # bias
+    assert L.vnm24_spmm(None, C.byref(a), 256, 8, fake, 256, 256, None, 0, fake, 256, None) == EINVAL    # colidx
+    assert L.vnm24_spmm(fake + 4, C.byref(a), 256, 8, fake, 256, 256, None, 0, fake, 256, None) == EALIGN
+    assert L.vnm24_spmm(fake, C.byref(a), 128, 8, fake, 256, 256, None, 0, fake, 256, None) == EUNS      # V % 256
+    assert L.vnm24_spmm(fake, C.byref(a), 256, 8, fake, 264, 264, None, 0, fake, 264, None) == EUNS      # N % 256
+    a2 = _sp(fake, fake, 512, 192, 96, 32, native)                                                      # 192 % 128
+    assert L.vnm24_spmm(fake, C.byref(a2), 256, 8, fake, 256, 256, None, 0, fake, 256, None) == EUNS
+
+
+def test_host_validation_of_the_hybrid_calls(native):
+    L = native.lib
+    EINVAL, EALIGN = native.P24_EINVAL, native.P24_EALIGN
+    fake = 0x10000  # never dereferenced: every call below fails validation first
+    H = native.p24_hybrid
+    good = dict(rows=8, cols=64, E=4, cap=2, nnz=fake, ell_cols=fake, ell_vals=fake, slot=fake, ovf_rows=fake,
+                n_ovf=fake, ovf=fake, ldo=64)
+    def h(**kw):
+        return H(**{**good, **kw})
+    assert L.hyb_compress(fake, 64, C.byref(h(cols=60)), None) == EINVAL          # cols % 8
+    assert L.hyb_compress(fake, 64, C.byref(h(cols=65544)), None) == EINVAL       # > 65536 columns
+    assert L.hyb_compress(fake, 64, C.byref(h(E=0)), None) == EINVAL
+    assert L.hyb_compress(fake, 64, C.byref(h(nnz=None)), None) == EINVAL
+    assert L.hyb_compress(fake, 64, C.byref(h(slot=fake + 2)), None) == EALIGN
+    assert L.hyb_compress(fake, 64, C.byref(h(ell_vals=fake + 4)), None) == EALIGN
+    assert L.hyb_compress(fake, 60, C.byref(h()), None) == EINVAL                 # lda < cols
+    assert L.hyb_spmm(C.byref(h()), fake, 12, 16, fake, 16, None) == EINVAL       # N % 8
+    assert L.hyb_sddmm(C.byref(h()), fake, 40000, 40000, fake, 40000, fake, fake, 64, None) == EINVAL  # N cap
+    assert L.hyb_sddmm(C.byref(h()), fake, 16, 16, fake, 16, fake + 2, fake, 64, None) == EALIGN

@@ -31,11 +31,14 @@ def P():
     return P
 
 
-def run_gpu(P, inp, act24, adapters=None):
+def run_gpu(P, inp, act24, adapters=None, vnm=None):
     M, ffn = inp["X"].shape[0], inp["W_up"].shape[0]
     dH = torch.empty((M, ffn), dtype=torch.bfloat16, device="cuda")
     o = P.ffn24_step(inp["X"], inp["W_up"], inp["b_up"], inp["W_down"], inp["b_down"], inp["dY"], act24=act24,
-                     adapters=adapters, out={"dH": dH})
+                     adapters=adapters, out={"dH": dH}, vnm=vnm)
+    if vnm is not None:
+        # the step's H before its V:2:M prune: the same deterministic up-forward kernel
+        o["H_pre"] = P.spmm24_fwd(inp["X"], P.prune24_compress(inp["W_up"]), bias=inp["b_up"], relu=True)
     torch.cuda.synchronize()
     assert P.p24_query_status() == 0
     return o
@@ -58,7 +61,59 @@ def act_flip_groups(Hg_bits, ref, ffn, scale, slack=None):
     return diff
 
 
-def validated_decisions(o, ref, w: FFNWorkload, act24: bool, slack=None):
+def vnm_flagged(o, ref, V: int, Mg: int, scale: float):
+    """V:N:M activations: [M, ffn] bool of the block-groups whose column selection the
+    GPU took differently, and the rows x groups whose 2:4 pick among the selected
+    columns differs, each validated as a decision on rounded values:
+      - selection: a column the GPU kept and the oracle did not, against one the oracle
+        kept and the GPU did not, must score equal (the oracle's fp32 L1 norms over the
+        block) within the two sides' pre-prune H difference summed over the block (the
+        GPU's pre-prune H comes from the same deterministic up-forward kernel) plus the
+        fp32 rounding of two sums of V terms;
+      - pick: the kept nonzero magnitudes must agree up to bf16 rounding, or differ by a
+        value within rounding of 0 (a ReLU-gate decision), as for 2:4 activations.
+    Returns (mask, number of flagged block-groups)."""
+    from oracle import vnm_oracle as VNM
+    Hg = bits_of(o["H"])
+    Hpre = bits_of(o["H_pre"])
+    Hr = ref["H"]
+    M, ffn = Hg.shape
+    G, nb = ffn // Mg, (M + V - 1) // V
+    scores = VNM.column_scores(Hr, V, Mg).astype(np.float64)                    # [nb, ffn]
+    dpre = np.abs(O.bf16_to_f32(Hpre).astype(np.float64) - O.bf16_to_f32(Hr))
+    slack = np.add.reduceat(dpre, np.arange(0, M, V), axis=0)                    # [nb, ffn]
+    rounding = 2 * V * 2.0 ** -24 * scores.max(axis=1, keepdims=True)
+    nzg = (Hg & np.uint16(0x7FFF)) != 0
+    nzr = (ref["H_used"] & np.uint16(0x7FFF)) != 0
+    sel_r = np.zeros((nb, G, Mg), bool)
+    np.put_along_axis(sel_r, ref["Hv_colidx"].astype(np.int64), True, axis=2)
+    used_g = np.zeros((nb, ffn), bool)
+    for b in range(nb):
+        used_g[b] = nzg[b * V:(b + 1) * V].any(axis=0)
+    used_g = used_g.reshape(nb, G, Mg)
+    flagged = np.zeros((M, ffn), bool)
+    n_sel = 0
+    for b, g in zip(*np.nonzero((used_g & ~sel_r).any(axis=2))):
+        extra = np.nonzero(used_g[b, g] & ~sel_r[b, g])[0] + g * Mg           # GPU-kept, not oracle-selected
+        lost = np.nonzero(sel_r[b, g] & ~used_g[b, g])[0] + g * Mg             # oracle-selected, unused by GPU
+        for a in extra:
+            gap = np.abs(scores[b, a] - scores[b, lost])
+            assert np.any(gap <= slack[b, a] + slack[b, lost] + rounding[b, 0]), (b, g, a, lost, gap)
+        flagged[b * V:(b + 1) * V, g * Mg:(g + 1) * Mg] = True
+        n_sel += 1
+    assert n_sel <= 16 + 1e-3 * nb * G, n_sel
+    # picks within an agreed selection
+    diff = ((nzg != nzr) & ~flagged).reshape(M, G, Mg).any(axis=2)
+    for m, g in zip(*np.nonzero(diff)):
+        h = np.abs(ref["H_ref"][m, g * Mg:(g + 1) * Mg])
+        kept_r = np.sort(np.r_[h[nzr[m, g * Mg:(g + 1) * Mg]], 0.0, 0.0])[-2:]
+        kept_g = np.sort(np.r_[h[nzg[m, g * Mg:(g + 1) * Mg]], 0.0, 0.0])[-2:]
+        assert np.allclose(kept_r, kept_g, rtol=2 ** -7, atol=1e-3 * scale), (m, g, h)
+        flagged[m, g * Mg:(g + 1) * Mg] = True
+    return flagged, n_sel
+
+
+def validated_decisions(o, ref, w: FFNWorkload, act24: bool, slack=None, vnm=None):
     """[M, ffn] bool: elements where the GPU and the oracle legitimately took a decision
     on a rounded value differently, each validated here:
       - ReLU gate [H > 0] where the pre-activation is within rounding of 0 (the
@@ -72,20 +127,24 @@ def validated_decisions(o, ref, w: FFNWorkload, act24: bool, slack=None):
     Hr = O.bf16_to_f32(ref["H_used"])
     flagged = np.zeros(Hg.shape, dtype=bool)
     scale = float(np.sqrt(np.mean(ref["H_ref"].astype(np.float64) ** 2))) or 1.0
+    sel_flagged = np.zeros(Hg.shape, dtype=bool)
     if act24:
         groups = act_flip_groups(bits_of(o["H"]), ref, w.ffn, scale, slack)
         flagged |= np.repeat(groups, 4, axis=1)
+    if vnm is not None:
+        sel_flagged, _ = vnm_flagged(o, ref, vnm[0], vnm[1], scale)
+        flagged |= sel_flagged
     gate = ((Hg > 0) != (Hr > 0)) & ~flagged
     near_zero = np.maximum(Hg, Hr)[gate]
     limit = 1e-3 * scale + (0.0 if slack is None else slack[gate])
     assert np.all(near_zero <= limit), (near_zero.max(), scale)
     flagged |= gate
-    n = int(flagged.sum())
+    n = int((flagged & ~sel_flagged).sum())
     assert n <= 16 + 1e-5 * flagged.size, n
-    return flagged, n
+    return flagged, int(flagged.sum())
 
 
-def compare_step(o, ref, w: FFNWorkload, act24: bool, adapters: dict | None = None):
+def compare_step(o, ref, w: FFNWorkload, act24: bool, adapters: dict | None = None, vnm=None):
     """Every output, every element, against the oracle's fp32 values: H and dH (the
     step's bf16 intermediates) at the plain tolerance outside the validated decisions;
     Y, dX, dW_up, dW_down and db_up at the plain tolerance plus the exact propagated
@@ -96,7 +155,7 @@ def compare_step(o, ref, w: FFNWorkload, act24: bool, adapters: dict | None = No
     slack = None
     if adapters is not None:   # H's pre-activation carries T_up's rounding through L_up
         slack = propagated(ulp_bf16(ref["T_up"]) ** 2, sq(adapters["L_up"]).T)
-    flagged, _ = validated_decisions(o, ref, w, act24, slack)
+    flagged, _ = validated_decisions(o, ref, w, act24, slack, vnm)
     absf = lambda a: np.abs(O.bf16_to_f32(a))  # noqa: E731
     Hd = delta_csr(bits_of(o["H"]), ref["H_used"])                      # [M, ffn]
     dHd = delta_csr(bits_of(o["dH"]), ref["dH"])                        # [M, ffn]
@@ -107,7 +166,7 @@ def compare_step(o, ref, w: FFNWorkload, act24: bool, adapters: dict | None = No
     cdWu = chained(dHd.T.tocsr(), absf(ref["X"]))                       # [ffn, d]
     cdbu = np.asarray(dHd.sum(axis=0)).ravel()                          # [ffn]
     cdWd = chained(Hd.T.tocsr(), absf(ref["dY"])).T                     # [d, ffn]
-    Hm = O.bf16_to_f32(ref["H_used"]) if act24 else ref["H_ref"]
+    Hm = O.bf16_to_f32(ref["H_used"]) if (act24 or vnm) else ref["H_ref"]
     eH = edH = eY = edX = None
     if adapters is not None:
         L_up2, R_up2, L_dn2, R_dn2 = (sq(adapters[k]) for k in ("L_up", "R_up", "L_down", "R_down"))
@@ -154,10 +213,11 @@ def compare_step(o, ref, w: FFNWorkload, act24: bool, adapters: dict | None = No
     assert np.all(bits_of(o["dW_down"])[~O.mask_from_meta(ref["down_meta"], w.ffn)] == 0)
 
 
-def oracle_step(inp, act24, adapters=None):
+def oracle_step(inp, act24, adapters=None, vnm=None):
     r = O.ffn_step(bits_of(inp["X"]), bits_of(inp["W_up"]), inp["b_up"].cpu().numpy(), bits_of(inp["W_down"]),
                    inp["b_down"].cpu().numpy(), bits_of(inp["dY"]), act24=act24,
-                   adapters=None if adapters is None else {k: bits_of(v) for k, v in adapters.items()})
+                   adapters=None if adapters is None else {k: bits_of(v) for k, v in adapters.items()},
+                   act_vnm=vnm)
     r["X"], r["dY"] = bits_of(inp["X"]), bits_of(inp["dY"])
     return r
 
@@ -406,3 +466,29 @@ def test_ffn_step_70b_m2048_adapters_in_full(P):
     ad = adapter_inputs(w, 64, seed=0)
     o = run_gpu(P, inp, False, ad)
     compare_step(o, oracle_step(inp, False, ad), w, False, {k: bits_of(v) for k, v in ad.items()})
+
+
+# ---------------------------------------------------------------- V:N:M activations
+@pytest.mark.parametrize("shape,Mg", [((512, 256, 1024), 8), ((4096, 768, 3072), 8), ((512, 256, 2048), 16)])
+def test_ffn_step_vnm_integer_inputs_bit_exact(P, shape, Mg):
+    """V:N:M activations (V = 256) on integer inputs: the column scores are exact integer
+    sums on both sides, so every decision and every output must agree bit for bit."""
+    M, d, ffn = shape
+    w = FFNWorkload("int", M, d, ffn, 1.0)
+    inp = integer_inputs(w, seed=7)
+    o = run_gpu(P, inp, False, vnm=(256, Mg))
+    ref = oracle_step(inp, False, vnm=(256, Mg))
+    assert np.abs(ref["dW_up_ref"]).max() < 2 ** 20 and np.abs(ref["dW_down_ref"]).max() < 2 ** 20
+    assert_bits_equal(bits_of(o["H"]), ref["H_used"], "H (V:2:M pruned)")
+    for k in ("Y", "dX", "dW_up", "dW_down"):
+        assert_bits_equal(bits_of(o[k]), ref[k], k)
+    assert np.array_equal(o["db_up"].cpu().numpy(), ref["db_up"])
+    assert np.array_equal(o["db_down"].cpu().numpy(), ref["db_down"])
+
+
+@pytest.mark.parametrize("name,Mg", [("gpt2", 8), ("1p3b", 8), ("gpt2", 16)])
+def test_ffn_step_vnm_workloads(P, name, Mg):
+    w = WORKLOADS[name]
+    inp = ffn_inputs(w, seed=0, device="cuda", bias=True)
+    o = run_gpu(P, inp, False, vnm=(256, Mg))
+    compare_step(o, oracle_step(inp, False, vnm=(256, Mg)), w, False, vnm=(256, Mg))

@@ -1,5 +1,6 @@
-"""GPU parity of the V:2:M prune (vnm24_compress) against the oracle: the kept
-column offsets, values, metadata and padding, bit for bit."""
+"""GPU parity of the V:2:M path against the oracle: the prune (vnm24_compress: kept
+column offsets, values, metadata, padding and the dense masked form, bit for bit)
+and the V:2:M GEMM (vnm24_spmm, within the stated tolerance)."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +9,7 @@ from oracle import prune24_oracle as O
 from oracle import vnm_oracle as VNM
 from synth24 import normal_bf16, small_int_bf16
 from tests.conftest import bits_of, from_bits
-from tests.p24_testutil import assert_bits_equal, sparse_bits
+from tests.p24_testutil import assert_bits_equal, assert_close, sparse_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -77,3 +78,77 @@ def test_vnm_m4_equals_2to4(P):
     torch.cuda.synchronize()
     for x, y, name in zip(sparse_bits(out), sparse_bits(ref), ("vals", "meta")):
         assert_bits_equal(x, y, name)
+
+
+@pytest.mark.parametrize("rows,cols,V,M", [(300, 1024, 256, 8), (40, 264, 16, 8), (9, 384, 4, 128),
+                                           (600, 512, 300, 8)])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_vnm_compress_masked_output(P, rows, cols, V, M, in_place):
+    """The dense masked form A_masked (A with every pruned entry +0), written beside the
+    compressed one or over A itself; bit-exact against the oracle's decompression.
+    V above 256 (the unstaged kernel) has no masked output: P24_EUNSUPPORTED."""
+    A = make_a(rows, cols, "specials", seed=rows + V)
+    Ab = bits_of(A)
+    if V > 256:
+        with pytest.raises(P.P24Error):
+            P.vnm24_compress(A, V, M, A_masked=torch.empty_like(A))
+        return
+    Am = A if in_place else torch.empty_like(A)
+    colidx, out = P.vnm24_compress(A, V, M, A_masked=Am)
+    torch.cuda.synchronize()
+    rc, rv, rm = VNM.vnm_compress(Ab, V, M)
+    assert np.array_equal(colidx.cpu().numpy(), rc), "colidx"
+    assert_bits_equal(bits_of(Am), VNM.vnm_decompress(rc, rv, rm, rows, cols, V, M), "A_masked")
+    gv, gm = sparse_bits(out)
+    rv2, rm2 = O.compress24(VNM.condense(Ab, rc, V, M), out.ldv, out.ldm)
+    assert_bits_equal(gv, rv2, "vals")
+    assert_bits_equal(gm, rm2, "meta")
+
+
+def oracle_vnm_operand(P, A_bits, V, M):
+    """The oracle's V:2:M form of A (colidx, condensed 2:4), uploaded for the GEMM."""
+    rows, cols = A_bits.shape
+    ci, _, _ = VNM.vnm_compress(A_bits, V, M)
+    s = P.Sparse24.empty(rows, 4 * cols // M)
+    v, m = O.compress24(VNM.condense(A_bits, ci, V, M), s.ldv, s.ldm)
+    s.vals.copy_(from_bits(v, "cuda"))
+    s.meta.copy_(torch.from_numpy(m).to("cuda"))
+    return torch.from_numpy(ci).to("cuda"), s, (ci, v, m)
+
+
+# (R rows of A, K, N, V, M): several tiles each way, a ragged last row block, V above 256, M from 4 to 32
+SPMM_CASES = [(512, 1024, 512, 256, 8), (700, 2048, 256, 256, 8), (768, 2048, 768, 512, 16),
+              (512, 512, 256, 256, 4), (256, 4096, 512, 256, 32)]
+
+
+@pytest.mark.parametrize("R,K,N,V,M", SPMM_CASES)
+@pytest.mark.parametrize("bias,relu", [(False, False), (True, True)])
+def test_vnm24_spmm(P, R, K, N, V, M, bias, relu):
+    """Y = act(A . B + bias), A V:2:M (the oracle's compression, uploaded), B [K, N]."""
+    from synth24 import normal_f32
+    A = bits_of(torch.relu(normal_bf16((R, K), 1.0, 7, 7)))
+    B = normal_bf16((K, N), 0.02, 7, 3, "cuda")
+    b = normal_f32((N,), 0.1, 7, 5, "cuda") if bias else None
+    ci, As, (rc, rv, rm) = oracle_vnm_operand(P, A, V, M)
+    Y = P.vnm24_spmm(ci, As, V, M, B, bias=b, relu=relu)
+    torch.cuda.synchronize()
+    assert P.p24_query_status() == 0
+    ref, _ = VNM.vnm_linear(rc, rv, rm, R, K, V, M, bits_of(B), bias=None if b is None else b.cpu().numpy(),
+                            relu=relu)
+    assert_close(Y, ref, "Y")
+
+
+def test_vnm24_spmm_70b_down_shape(P):
+    """The down linear of the 70B FFN fed V:N:M activations (256:2:8): A = H [16384,
+    28672], B = W_down^T [28672, 8192]. Checked on two whole row blocks (512 rows)."""
+    R, K, N, V, M = 16384, 28672, 8192, 256, 8
+    A = bits_of(torch.relu(normal_bf16((R, K), 1.0, 8, 7)))
+    B = normal_bf16((K, N), 0.01, 8, 3, "cuda")
+    ci, As, (rc, rv, rm) = oracle_vnm_operand(P, A, V, M)
+    Y = P.vnm24_spmm(ci, As, V, M, B)
+    torch.cuda.synchronize()
+    assert P.p24_query_status() == 0
+    for blk in (3, 41):
+        rows = slice(blk * V, (blk + 1) * V)
+        ref, _ = VNM.vnm_linear(rc[blk:blk + 1], rv[rows], rm[rows], V, K, V, M, bits_of(B))
+        assert_close(Y[rows], ref, f"Y block {blk}")
