@@ -75,6 +75,8 @@ struct SpmmParams {
   // offset j). B is K-outer [vnm_K rows, rowsB columns]; stage rows are gathered by TMA.
   const uint32_t* vnm_cix;
   int vnm_group, vnm_V, vnm_G, vnm_K;
+  const uint16_t* vnm_B;  // B [vnm_K, vnm_ldb] (the rows the gather warps copy)
+  int64_t vnm_ldb;
 };
 
 struct DwParams {
@@ -183,7 +185,7 @@ struct SpmmSmem {
   static constexpr int kOffStage = kOffE + kEBufs * kE;  // epilogue transpose, 4 warps x 32x32 bf16
   static constexpr int kOffGate = kOffStage + 4 * 32 * 32 * 2;  // gate words: 4 warps x BN tokens x 32 features
   static constexpr int kOffBar = kOffGate + 4 * BN * 4;
-  static constexpr int kBytes = kOffBar + 8 * (3 * STAGES + 2 * kEBufs + 5) + 16;
+  static constexpr int kBytes = kOffBar + 8 * (4 * STAGES + 2 * kEBufs + 5) + 16;
   static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
   static constexpr int kTxDense = 2 * (kA + kBHalf);  // a dense stage: A_l 128 x 64, B_l BN/2 x 64 per CTA
 };
@@ -226,17 +228,45 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-// Four rows y0..y3 of a 2-D map (box: 64 columns x 1 row), columns x..x+63, land as
-// four consecutive 128-byte rows at dst (the map's swizzle applies, as for a tile
-// load); the bytes complete on the pair leader's barrier.
-__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y0,
-                                                 int y1, int y2, int y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-      : "memory");
+// ---- gathered B (V:2:M): 16-byte copies by threads, tracked on an mbarrier
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed (the
+// barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Bounded wait with cluster-scope acquire: pairs with a peer CTA's release arrive.
+__device__ __forceinline__ bool p24_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 255u) == 255u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > P24_WAIT_NS) {
+        *abort = 1;
+        p24_record_timeout(status, bar);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void arrive_cluster_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -269,7 +299,7 @@ enum SpmmEpi : int {
 };
 
 template <int BN, int STAGES, bool kTransOut, int kEpi, bool kGather = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 448 : 320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmL,
                 const __grid_constant__ CUtensorMap tmT, const SpmmParams p) {
@@ -296,7 +326,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   uint64_t* acc_full = eempty + kEBufs;                               // [2] leader's commit, both CTAs
   uint64_t* acc_empty = acc_full + 2;                                 // [2] leader's is used (8 arrivals)
   uint64_t* spare = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(spare + 1);
+  uint64_t* bfull = spare + 1;                                        // [STAGES] gathered B: own copies landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfull + STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -304,9 +335,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // gathered B: the leader's `full` also takes the peer's relay arrival
+      mbar_init(&full[s], kGather ? 2 : 1);
       mbar_init(&empty[s], 1);
       mbar_init(&meta_ready[s], 8);  // 4 mover warps x 2 CTAs
+      if (kGather) mbar_init(&bfull[s], 128);  // one arrival per gather thread
     }
     for (int e = 0; e < kEBufs; ++e) {
       mbar_init(&efull[e], 1);
@@ -341,78 +374,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
-  if (warp == 0 && kGather) {
-    // ------------------------------------------------ TMA producer, gathered B (whole warp, both CTAs)
-    // Per stage (128 condensed K = 32 groups of 4 selected columns): lane 0 loads A and
-    // the metadata like the plain producer; lane l gathers group 32 kb + l's 4 rows of
-    // B (its columns of this CTA's half of the tile), one gather4 per 64 columns.
-    uint32_t it = 0, eit = 0;
+  if (kGather && warp >= 10) {
+    // ------------------------------------------------ gather warps (both CTAs, gathered B)
+    // Stage rows (128 condensed K = 32 groups of 4 selected rows of M) are copied as 16
+    // pieces of 16 bytes (this CTA's 128 columns): thread th takes piece c = th % 16 of
+    // rows r = 8 i + th / 16, i < 16, so a half warp reads one row's 256 bytes. Row r is
+    // row (32 kb + r / 4) M + colidx byte r % 4 of B; its piece c lands in atom c / 8,
+    // chunk (c % 8) ^ (r % 8) of the 128B-swizzled MN-major layout. Each thread then
+    // arrives once on bfull[s] when its copies have landed.
+    const int th = threadIdx.x - 320;
+    const int c = th & 15;
+    const uint32_t sh = 8u * static_cast<uint32_t>((th >> 4) & 3);  // colidx byte of this thread's rows
+    const int gofs = th >> 6;                                       // its rows' group within a pair of groups
+    uint32_t it = 0;
     bool ok = true;
     for (int t = cid; t < p.num_tiles && ok; t += ncl) {
       int ta, tb;
       tile_coords(t, p.tilesA, p.tilesB, p.group, ta, tb);
-      const uint32_t* cix = p.vnm_cix + static_cast<int64_t>((ta * 2 * kBM) / p.vnm_V) * p.vnm_G;
-      ta = 2 * ta + rank;
-      const int n0 = tb * BN + rank * (BN / 2);
-      // this lane's group offsets for the next kPf stages, loaded kPf stages ahead: when the
-      // gathers limit the pipeline the ring never fills, so a shorter distance would put an
-      // L2 round trip into every stage
-      constexpr int kPf = 4;
-      uint32_t c4r[kPf];
+      const uint32_t* cix = p.vnm_cix + static_cast<int64_t>((ta * 2 * kBM) / p.vnm_V) * p.vnm_G + gofs;
+      const uint16_t* bsrc = p.vnm_B + tb * BN + rank * (BN / 2) + 8 * c;
+      const uint32_t dst0 = smem_u32(smem + L::kOffB) + (c >> 3) * 16384u;
+      uint32_t cw[16];  // colidx words of this thread's 16 rows for the current stage
 #pragma unroll
-      for (int j = 0; j < kPf; ++j) c4r[j] = j < p.nkb ? __ldg(cix + 32 * j + lane) : 0u;
-      for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kPf) {
-#pragma unroll
-      for (int jj = 0; jj < kPf; ++jj) {
-        const int kb = kb0 + jj;
-        if (kb >= p.nkb) break;
+      for (int i = 0; i < 16; ++i) cw[i] = __ldg(cix + 2 * i);
+      for (int kb = 0; kb < p.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        const uint32_t c4 = c4r[jj];
-        int good = 1;
-        if (kb % kEStages == 0) {  // next metadata block
-          const int e = eit % kEBufs;
-          if (lane == 0) {
-            good = p24_wait(&eempty[e], ((eit / kEBufs) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
-            if (good) {
-              mbar_arrive_expect_tx(&efull[e], L::kE);
-              tma_load_2d(smem + L::kOffE + e * L::kE, &tmE, &efull[e], (kb / kEStages) * 64, ta * kBM);
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
-          ++eit;
-        }
-        if (lane == 0) good = p24_wait(&empty[s], ph ^ 1, abort_flag, p.status) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
-        const uint32_t fullL = leader_addr(&full[s]);
-        if (lane == 0) {
-          if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
-          tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 64, ta * kBM);
-        }
-        const int g = kb * 32 + lane;  // every stage is full: the host requires 128 | condensed K
-        const int yb = g * p.vnm_group;
-        const int y0 = yb + static_cast<int>(c4 & 0xFFu), y1 = yb + static_cast<int>((c4 >> 8) & 0xFFu);
-        const int y2 = yb + static_cast<int>((c4 >> 16) & 0xFFu), y3 = yb + static_cast<int>(c4 >> 24);
-        c4r[jj] = (kb + kPf < p.nkb) ? __ldg(cix + g + 32 * kPf) : 0u;
-        uint8_t* bst = smem + L::kOffB + s * L::kB + lane * 512;
+        if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t dst = dst0 + static_cast<uint32_t>(s * L::kB);
+        const int gb = kb * 32 + gofs;  // every stage is full: the host requires 128 | condensed K
 #pragma unroll
-        for (int a = 0; a < BN / 128; ++a) tma_gather4_pair(bst + a * 16384, &tmB, fullL, n0 + a * 64, y0, y1, y2, y3);
-        __syncwarp();
-        ++it;
-      }
+        for (int i = 0; i < 16; ++i) {
+          const int r = 8 * i + (th >> 4);
+          const int y = (gb + 2 * i) * p.vnm_group + static_cast<int>((cw[i] >> sh) & 0xFFu);
+          cp_async_16(dst + static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(c & 7) ^ static_cast<uint32_t>(r & 7)) << 4),
+                      bsrc + static_cast<int64_t>(y) * p.vnm_ldb);
+        }
+        cp_async_arrive(&bfull[s]);
+        if (kb + 1 < p.nkb) {  // the next stage's words, loaded while this stage's copies fly
+#pragma unroll
+          for (int i = 0; i < 16; ++i) cw[i] = __ldg(cix + (kb + 1) * 32 + 2 * i);
+        }
       }
     }
-    // Drain: the last issued loads must land before the CTA may exit.
+    cp_async_wait_all();  // this thread's copies land before the CTA may exit
+  } else if (warp == 1 && kGather && !leader) {
+    // ------------------------------------------------ relay (second CTA of a gathering pair)
+    // This CTA's gathered B for stage s is complete: order it for the tensor cores (async
+    // proxy) and tell the leader, whose MMAs read it, with a cluster-scope release.
     if (lane == 0) {
-      const uint32_t n_drain = it < STAGES ? it : STAGES;
-      for (uint32_t i = 0; i < n_drain; ++i) {
-        const uint32_t j = it - 1 - i;
-        if (leader) p24_wait_quiet(&full[j % STAGES], (j / STAGES) & 1);
-      }
-      const uint32_t e_drain = eit < kEBufs ? eit : kEBufs;
-      for (uint32_t i = 0; i < e_drain; ++i) {
-        const uint32_t j = eit - 1 - i;
-        p24_wait_quiet(&efull[j % kEBufs], (j / kEBufs) & 1);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cid; t < p.num_tiles && ok; t += ncl) {
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!p24_wait(&bfull[s], (it / STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
+          fence_proxy_async_cta();
+          arrive_cluster_release(leader_addr(&full[s]));
+        }
       }
     }
   } else if (warp == 0) {
@@ -450,10 +469,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             ++eit;
           }
           if (!p24_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (leader) mbar_arrive_expect_tx(&full[s], L::kTxPair);
+          if (leader) mbar_arrive_expect_tx(&full[s], kGather ? 2 * L::kA : L::kTxPair);
           const uint32_t fullL = leader_addr(&full[s]);
           tma_load_2d_pair(smem + L::kOffA + s * L::kA, &tmA, fullL, kb * 64, ta * kBM);
-          if (p.b3d) {
+          if (kGather) {
+            // B comes from the gather warps
+          } else if (p.b3d) {
             tma_load_3d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, 0, tb * BN + rank * (BN / 2), kb * 2);
           } else {
             tma_load_2d_pair(smem + L::kOffB + s * L::kB, &tmB, fullL, kb * 128, tb * BN + rank * (BN / 2));
@@ -488,8 +509,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         for (int kb = 0; kb < nstages; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!p24_wait(&full[s], ph, abort_flag, p.status) ||
-              !p24_wait(&meta_ready[s], ph, abort_flag, p.status)) {
+          if (kGather) {
+            // A (TMA) and the peer's gathered B (cluster release) on `full`, this CTA's
+            // gathered B on `bfull`; then order the copies for the tensor cores
+            if (!p24_wait_cluster(&full[s], ph, abort_flag, p.status) ||
+                !p24_wait(&bfull[s], ph, abort_flag, p.status) ||
+                !p24_wait(&meta_ready[s], ph, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_cta();
+          } else if (!p24_wait(&full[s], ph, abort_flag, p.status) ||
+                     !p24_wait(&meta_ready[s], ph, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -531,7 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       }
       __syncwarp();
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------ metadata movers (both CTAs)
     // Lane l of quarter q fills TMEM lane 32q + l: rows rA = 32q + (l & 16) + (l & 7)
     // and rA + 8, K-half h = (l >> 3) & 1 of each MMA's 32 metadata bits.
@@ -1096,13 +1127,14 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   using L = SpmmSmem<BN, kSpStages>;
   auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi, kGather>;
   const int smem = L::kBytes + 1024;
+  constexpr int kThreads = kGather ? 448 : 320;  // + 4 gather warps
   static LaunchSetup setup;
   int clusters = 0;
-  cudaError_t err = launch_setup(setup, kern, 2, 320, smem, clusters);
+  cudaError_t err = launch_setup(setup, kern, 2, kThreads, smem, clusters);
   if (err != cudaSuccess) return err;
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
-  kern<<<grid, 320, smem, s>>>(a, b, e, l, t, p);
+  kern<<<grid, kThreads, smem, s>>>(a, b, e, l, t, p);
   count_launch();
   return cudaGetLastError();
 }
@@ -1233,14 +1265,15 @@ cudaError_t launch_vnm_spmm(const uint8_t* colidx, const p24_sparse& A, int V, i
   p.vnm_V = V;
   p.vnm_G = static_cast<int>(K / Mg);
   p.vnm_K = static_cast<int>(K);
+  p.vnm_B = static_cast<const uint16_t*>(B);
+  p.vnm_ldb = ldb;
   CUtensorMap ta, tb, te;
   if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A.vals, A.cols / 2, A.rows, A.ldv * 2, 64, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.meta, A.ldm, A.rows, A.ldm, 16 * kEStages, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      // B [K, N]: one-row boxes of 64 columns, the gather4 form
-      !make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, ldb * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  tb = ta;  // B is gathered by the kernel's threads (p.vnm_B), not by TMA
   return run_spmm<kSpBNWide, false, kEpiStore, true>(ta, tb, te, ta, tb, p, s);
 }
 
