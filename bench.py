@@ -50,17 +50,18 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def captured_traffic(workload: str) -> float | None:
-    """Per-launch DRAM bytes (read + write) of spmm_kernel at this workload, or None
-    when no capture matches the current kernel sources."""
+def captured_traffic(workload: str) -> tuple[float | None, str | None]:
+    """Per-launch DRAM bytes (read + write) of spmm_kernel at this workload and how they
+    were obtained, or (None, None) when no capture matches the current kernel sources."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, None
     if rec.get("kernel_source_sha256") != kernel_source_hash():
-        return None
-    return rec.get("per_launch_bytes", {}).get(workload)
+        return None, None
+    v = rec.get("per_launch_bytes", {}).get(workload)
+    return v, (None if v is None else rec.get("scaling"))
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -215,6 +216,38 @@ def cpu_baseline(w, seconds_target: float = 15.0) -> dict:
                        f"median of {len(times)} runs, {t:.2f} s each")}
 
 
+# ------------------------------------------------------------------ end to end, per configuration
+def config_e2e(P, cw, ci: dict, co: dict, dev, stream, args) -> dict:
+    """The configuration's step fed from pinned host buffers through StepPipeline: the
+    inputs (X, W_up, W_down, dY) copied in and the results (Y, dX, dW_up, dW_down, db)
+    copied out every step, overlapped with neighbouring steps' compute."""
+    from semi_structured_sparse_prune24_gb300.pipeline import StepPipeline
+    hin = {k: ci[k].cpu().pin_memory() for k in ("X", "W_up", "W_down", "dY")}
+    hout = {k: torch.empty(co[k].shape, dtype=co[k].dtype).pin_memory()
+            for k in ("Y", "dX", "dW_up", "dW_down", "db_up", "db_down")}
+    pipe = StepPipeline(cw.M, cw.d, cw.ffn, act24=cw.act24, b_up=ci["b_up"], b_down=ci["b_down"], device=dev)
+    for _ in range(args.warmup):
+        pipe.submit(hin, hout)
+    pipe.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    pipe.start_after(e0)
+    for _ in range(args.steps):
+        pipe.submit(hin, hout)
+    pipe.finish_on(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if P.p24_query_status() != 0:
+        raise RuntimeError("device status word set during the end-to-end steps")
+    ems = e0.elapsed_time(e1) / args.steps
+    out = {"value": cw.dense_equiv_flop / (ems * 1e-3) / 1e12, "unit": "TFLOPS (dense-equivalent)",
+           "ms_per_step": ems, "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+           "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout.values())}
+    del pipe, hin, hout
+    return out
+
+
 # ------------------------------------------------------------------ hybrid activations
 def bench_hybrid(P, dev, stream, seed, args, peaks) -> dict:
     """The hybrid ELL + dense-overflow path on synthetic ReLU activations: z ~ N(0, 1)
@@ -261,9 +294,13 @@ def bench_hybrid(P, dev, stream, seed, args, peaks) -> dict:
     t_d = timed(lambda: P.hyb_sddmm(h, G, Wt, S_ell=S_ell, S_ovf=S_ovf))
     t_dense = timed(lambda: P.p24_gemm_nt(H, Wd, C_out=Yd))
     # L2-resident copy (16 MB each way) as the reference for the gathers
-    a = torch.empty(8 * 2 ** 20, dtype=torch.bfloat16, device=dev)
+    a = torch.empty(16 * 2 ** 20, dtype=torch.bfloat16, device=dev)    # 32 MB, twice: L2-resident
     bcopy = torch.empty_like(a)
-    t_l2 = timed(lambda: bcopy.copy_(a))
+
+    def copies():
+        for _ in range(20):
+            bcopy.copy_(a)
+    t_l2 = timed(copies) / 20
     l2_gbs = 2 * a.numel() * 2 / (t_l2 * 1e-3) / 1e9
     if P.p24_query_status() != 0:
         raise RuntimeError("device status word set during the hybrid timings")
@@ -283,7 +320,7 @@ def bench_hybrid(P, dev, stream, seed, args, peaks) -> dict:
            "dense_tensor_core_same_product_ms": t_dense,
            "l2_copy_GBs": l2_gbs,
            "note": "gathered bytes = nonzeros x d x 2 (one W_down^T row per nonzero); the L2 figure is a "
-                   "16 MB copy measured in this run"}
+                   "32 MB L2-resident copy measured in this run"}
     del H, Wt, Wd, G, h, Y, S_ell, S_ovf, Yd, a, bcopy
     return out
 
@@ -378,7 +415,8 @@ def run_ours(args, world, rank, local):
     dk = kernels[dominant]
     roofline = {"kernel": dominant, "bound": dk["bound"], "achieved": breakdown[dominant]["achieved"],
                 "peak": dk["peak"], "unit": dk["unit"], "frac": breakdown[dominant]["frac"],
-                "traffic": captured_traffic(args.workload) if dominant.startswith("spmm_kernel") else None,
+                "traffic": captured_traffic(args.workload)[0] if dominant.startswith("spmm_kernel") else None,
+                "traffic_source": captured_traffic(args.workload)[1] if dominant.startswith("spmm_kernel") else None,
                 "peak_source": f"{peak_src} bf16_tflops_sustained" +
                                (" x 2 (nominal 2:4 ratio)" if dk["peak"] == sparse_peak else "")
                                if dk["unit"] == "TFLOP/s" else f"{peak_src} hbm_gbs"}
@@ -547,7 +585,8 @@ def run_ours(args, world, rank, local):
                                                   act24=cw.act24, out=co, workspace=cws))
             cv = cw.dense_equiv_flop / (cms * 1e-3) / 1e12
             configs[cw.name] = {"ms_per_step": cms, "value": cv, "pct_sparse_peak": cv / sparse_peak,
-                                "dense_equiv_flop": cw.dense_equiv_flop}
+                                "dense_equiv_flop": cw.dense_equiv_flop,
+                                "e2e": config_e2e(P, cw, ci, co, dev, stream, args)}
             del ci, cws, co
         # single linears (prune + forward + double-pruned dX + masked dW): the 70B tail
         # shape and the tiny check
