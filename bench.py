@@ -504,7 +504,7 @@ def run_ours(args, world, rank, local):
             p1.record(stream)
             torch.cuda.synchronize(dev)
             pms = p0.elapsed_time(p1) / args.steps
-            per_elt = 2 + 2 + 4 / VM * 0.5 + 4 / VM / 8 + 4 / (VV * VM)   # read, masked write, values, nibbles, offsets
+            per_elt = 2 + 2 + 4 / VM + 0.5 / VM + 4 / (VV * VM)   # read, masked write, values, nibbles, offsets
             gbs = per_elt * Hv.numel() / (pms * 1e-3) / 1e9
             vnm["prune_H"] = {"ms": pms, "value": gbs, "unit": "GB/s", "frac_hbm": gbs / peaks["hbm_gbs"],
                               "algorithmic_bytes_per_elt": per_elt, "shape": [w.M, w.ffn]}

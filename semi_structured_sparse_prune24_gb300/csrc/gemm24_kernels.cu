@@ -1142,9 +1142,10 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
 }  // namespace
 
 bool make_tensor_map_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t inner, uint64_t outer,
-                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
   return make_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, bf16 ? 2 : 1, base,
-                     inner, outer, row_bytes, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_NONE);
+                     inner, outer, row_bytes, box_inner, box_outer,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64_t ldb, void* out, int64_t ldo,

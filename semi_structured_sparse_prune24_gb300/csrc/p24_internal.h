@@ -96,10 +96,11 @@ cudaError_t launch_hyb_spmm(const p24_hybrid& h, const void* B, int64_t N, int64
 cudaError_t launch_hyb_sddmm(const p24_hybrid& h, const void* G, int64_t N, int64_t ldg, const void* B, int64_t ldb,
                              void* S_ell, void* S_ovf, int64_t lds, cudaStream_t s);
 
-// A 2-D tensor map (no swizzle) over a row-major matrix, for the HBM-bound kernels'
-// TMA staging: `inner` columns of `outer` rows, boxes of box_inner x box_outer.
+// A 2-D tensor map over a row-major matrix, for the HBM-bound kernels' TMA staging:
+// `inner` columns of `outer` rows, boxes of box_inner x box_outer; swizzle128 lays each
+// 128-byte box row out with the 128B swizzle (box_inner x element size must be 128).
 bool make_tensor_map_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t inner, uint64_t outer,
-                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128 = false);
 
 int* device_status_ptr();  // the status word of the current device
 

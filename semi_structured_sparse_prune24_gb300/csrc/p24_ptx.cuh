@@ -53,6 +53,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete may be
+// suspended for up to `hint_ns` (woken earlier when the phase completes), so waiting
+// warps leave the issue slots to the warps that are working.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Bounded wait for the phase with parity `parity` to complete.
 // abort: CTA-shared flag; status: device status word.
 // Status block (int[4]): [0] P24_OK or P24_ETIMEOUT; for the first expired wait,
@@ -89,6 +109,20 @@ __device__ __forceinline__ bool p24_wait_for(uint64_t* bar, uint32_t parity, uin
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) {
+      p24_record_timeout(status, bar);
+      return false;
+    }
+  }
+}
+
+// p24_wait_for for waits that are expected to last: the thread is suspended in
+// between polls (see mbar_try_wait_hint).
+__device__ __forceinline__ bool p24_wait_for_idle(uint64_t* bar, uint32_t parity, uint64_t limit_ns, int* status) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_hint(a, parity, 20000u)) return true;
+    if ((i & 15u) == 15u && global_ns() - t0 > limit_ns) {
       p24_record_timeout(status, bar);
       return false;
     }

@@ -341,6 +341,272 @@ __global__ void __launch_bounds__(256) vnm_compress_staged_kernel(
   }
 }
 
+// V:2:M prune for groups of M <= 32 columns: persistent, TMA-fed, two tile buffers,
+// warp-specialised so that the serial column sums of one item overlap the prune of
+// the previous one.
+// Work item = (block of V rows, 64 * CWB columns), loaded as CWB boxes [V][64] with
+// the 128B swizzle: the 16-byte chunk c of row r sits at chunk c ^ (r & 7) of its
+// 128-byte row, so a warp reading the same columns of 8 rows, or whole rows, meets
+// no bank conflict. (CWB = 2 for V <= 128: each serial column pass then covers as
+// many bytes as one pass over 256 rows.)
+//   norm warps (64 * CWB threads), item k: column norms over the block, rows in
+//     order (fp32, sequential: the oracle's order), one column per thread; per group
+//     the 4 columns of largest norm (ties: lower column), their slots and byte
+//     offsets in a row, and for each 2:4 outcome a table of byte selectors that builds
+//     the group's dense masked form from the kept pair; then stage k & 1 is published.
+//   unit warps (256 threads), item k - 1 meanwhile: thread -> (row, group), the group
+//     fixed for the item and the rows 256 / (groups per row) apart (a multiple of 8,
+//     so the swizzle of the thread's rows is fixed too): the 4 kept values are read
+//     from shared memory, 2:4 among them gives the packed pair and the metadata nibble
+//     (a pair of groups is joined across neighbouring lanes), and the masked group --
+//     zeros with the two survivors in place -- is written straight from registers.
+//     M = 4 keeps every column: thread -> (row, two groups), one 16-byte chunk.
+//   When the unit warps are done with item k, their first thread refills the buffer
+//   with item k + 2. Stage k & 1 is rewritten only for item k + 2, whose tile cannot
+//   arrive before that point, so the stages need no barrier of their own.
+template <int M, int CWB>
+__global__ void __launch_bounds__(64 * CWB + 256) vnm_prune_swz_kernel(
+    const __grid_constant__ CUtensorMap tmA, int64_t rows, int64_t cols, int V, int sub_bytes, int64_t n_items,
+    int64_t nbx, uint8_t* __restrict__ colidx, uint16_t* __restrict__ vals, int64_t ldv,
+    uint8_t* __restrict__ meta, int64_t ldm, uint16_t* Am, int64_t ldam, int* status) {
+  static_assert(M >= 4 && M <= 32 && (M & (M - 1)) == 0, "groups of 4, 8, 16 or 32 columns");
+  static_assert(CWB == 1 || CWB == 2, "one or two 64-column boxes per item");
+  constexpr int CW = 64 * CWB;              // columns per item
+  constexpr int GR = M == 4 ? 8 : 64 / M;   // thread units per 64-column box row
+  constexpr int UR = GR * CWB;              // thread units per item row
+  constexpr int RSTEP = 256 / UR;           // rows between a unit thread's units
+  constexpr int MW = M / 2;                 // 32-bit words per group
+  constexpr int kNormThreads = CW;
+  constexpr int kUnitThreads = 256;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(4) uint8_t offs[2][CW];   // [stage][group][slot]: kept column within the group
+  __shared__ __align__(4) uint8_t boff[2][CW];   // [stage][group][slot]: its byte offset in a box row, unswizzled
+  __shared__ __align__(16) uint16_t mtab[2][M == 4 ? 8 : 512 * CWB];  // [stage][group][nibble][word]
+  __shared__ __align__(8) uint64_t full[2];
+  __shared__ __align__(8) uint64_t sel_full[2];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int t = threadIdx.x;
+  const int64_t G = cols / M;
+  const int buf_bytes = CWB * sub_bytes;
+  auto load = [&](int64_t it, int q) {
+    mbar_arrive_expect_tx(&full[q], static_cast<uint32_t>(CWB * V * 128));
+#pragma unroll
+    for (int j = 0; j < CWB; ++j)
+      tma_load_2d(tiles + q * buf_bytes + j * sub_bytes, &tmA, &full[q], static_cast<int>((it % nbx) * CW + 64 * j),
+                  static_cast<int>((it / nbx) * V));
+  };
+  if (t == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&sel_full[0], 1);
+    mbar_init(&sel_full[1], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (t == 0) {
+    load(blockIdx.x, 0);
+    if (blockIdx.x + gridDim.x < n_items) load(blockIdx.x + gridDim.x, 1);
+  }
+  if (t < kNormThreads) {
+    // ------------------------------------------------------------ norm warps
+    for (int64_t item = blockIdx.x, k = 0; item < n_items; item += gridDim.x, ++k) {
+      const int q = static_cast<int>(k & 1);
+      if (!p24_wait_for_idle(&full[q], static_cast<uint32_t>(k >> 1) & 1u, P24_WAIT_NS, status)) return;
+      const int64_t b = item / nbx;
+      const int64_t c0 = (item % nbx) * CW;
+      const int nr = static_cast<int>(min(rows - b * V, static_cast<int64_t>(V)));
+      const int ncol = static_cast<int>(min(static_cast<int64_t>(CW), cols - c0));  // multiple of 8 and of M
+      if (M == 4) {
+        // every column is kept (byte stores: the caller's colidx needs no alignment)
+        if (t < ncol) colidx[(b * G + c0 / 4) * 4 + t] = static_cast<uint8_t>(t & 3);
+      } else {
+        const uint8_t* tile = tiles + q * buf_bytes + (t >> 6) * sub_bytes;
+        const int cl = t & 63;  // column within its box
+        // column norms, one column per thread: 16 rows' loads issued ahead of their
+        // sequential additions (|x| is the value with its sign bit cleared)
+        uint32_t kt = 0;
+        if (t < ncol) {
+          const int cb = (cl >> 3) << 4, cw = (cl & 7) * 2;
+          float sum = 0.f;
+          int r = 0;
+          for (; r + 16 <= nr; r += 16) {
+            uint32_t x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              x[j] = *reinterpret_cast<const uint16_t*>(tile + (r + j) * 128 + (cb ^ ((j & 7) << 4)) + cw);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sum += fabsf(__uint_as_float(x[j] << 16));
+          }
+          for (; r < nr; ++r)
+            sum += fabsf(__uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(
+                                             tile + r * 128 + (cb ^ ((r & 7) << 4)) + cw))
+                                         << 16));
+          kt = (sum != sum) ? 0x7FC00000u : __float_as_uint(sum);
+        }
+        // the 4 kept columns of each group (ties: lower column): a group of M <= 32
+        // columns lies inside one warp, so the keys come by shuffle and the slots by ballot
+        const int lane = t & 31, j = t % M, gl0 = lane - j;
+        int beat = 0;
+#pragma unroll
+        for (int c = 0; c < M; ++c) {
+          const uint32_t kc = __shfl_sync(0xFFFFFFFFu, kt, gl0 + c);
+          beat += (kc > kt || (kc == kt && c < j)) ? 1 : 0;
+        }
+        const bool kp = t < ncol && beat < 4;
+        const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
+        const uint32_t gmask = (M == 32 ? 0xFFFFFFFFu : ((1u << M) - 1u)) << gl0;
+        if (kp) {
+          const int slot = __popc(km & gmask & ((1u << lane) - 1u));
+          offs[q][(t / M) * 4 + slot] = static_cast<uint8_t>(j);
+          boff[q][(t / M) * 4 + slot] = static_cast<uint8_t>(((cl >> 3) << 4) | ((cl & 7) << 1));
+          colidx[(b * G + (c0 + t) / M) * 4 + slot] = static_cast<uint8_t>(j);
+        }
+        __syncwarp();
+        // masked-group selectors: entry (group, nibble), word w takes from the kept pair
+        // (v0 in bytes 0-1, v1 in bytes 2-3) whichever survivor sits in column 2w (low
+        // half) and 2w + 1 (high half); byte 4 reads the zero operand. The lanes of a
+        // group share its 16 entries.
+        if (t < ncol) {
+          const int g = t / M;
+          for (int nb2 = j; nb2 < 16; nb2 += M) {
+            const int i0 = nb2 & 3, i1 = nb2 >> 2;
+            const int s0 = i0 < i1 ? offs[q][g * 4 + i0] : -1, s1 = i0 < i1 ? offs[q][g * 4 + i1] : -1;
+#pragma unroll
+            for (int w = 0; w < MW; ++w) {
+              const uint32_t lo = (s0 == 2 * w) ? 0x10u : (s1 == 2 * w) ? 0x32u : 0x44u;
+              const uint32_t hi = (s0 == 2 * w + 1) ? 0x10u : (s1 == 2 * w + 1) ? 0x32u : 0x44u;
+              mtab[q][(g * 16 + nb2) * MW + w] = static_cast<uint16_t>(lo | (hi << 8));
+            }
+          }
+        }
+      }
+      named_bar_sync(2, kNormThreads);
+      if (t == 0) mbar_arrive(&sel_full[q]);
+    }
+    return;
+  }
+  // -------------------------------------------------------------- unit warps
+  const int tu = t - kNormThreads;
+  const int lane = tu & 31;
+  const int u = tu % UR, rt = tu / UR;    // this thread's unit and first row
+  const int sw = (rt & 7) << 4;           // the swizzle of all its rows
+  const int nk = (V + RSTEP - 1) / RSTEP; // units per thread per item (uniform)
+  const int ub = (u / GR) * sub_bytes;    // the unit's box within a buffer
+  for (int64_t item = blockIdx.x, k = 0; item < n_items; item += gridDim.x, ++k) {
+    const int q = static_cast<int>(k & 1);
+    const uint32_t par = static_cast<uint32_t>(k >> 1) & 1u;
+    if (!p24_wait_for_idle(&sel_full[q], par, P24_WAIT_NS, status)) return;
+    if (!p24_wait_for(&full[q], par, P24_WAIT_NS, status)) return;
+    const uint8_t* tile = tiles + q * buf_bytes + ub;
+    const int64_t b = item / nbx;
+    const int64_t c0 = (item % nbx) * CW;
+    const int64_t r0 = b * V;
+    const int nr = static_cast<int>(min(rows - r0, static_cast<int64_t>(V)));
+    const int ncol = static_cast<int>(min(static_cast<int64_t>(CW), cols - c0));
+    const int uvalid = M == 4 ? ncol / 8 : ncol / M;
+    const int64_t g_first = c0 / M;
+    if (M == 4) {
+      const uint8_t* p = tile + rt * 128 + (((u % GR) << 4) ^ sw);
+      for (int kk = 0; kk < nk; ++kk) {
+        const int r = rt + kk * RSTEP;
+        if (r < nr && u < uvalid) {
+          const uint4 v = *reinterpret_cast<const uint4*>(p + kk * RSTEP * 128);
+          const uint32_t n0 = pick2_nibble(v.x, v.y), n1 = pick2_nibble(v.z, v.w);
+          *reinterpret_cast<uint2*>(vals + (r0 + r) * ldv + 2 * (g_first + 2 * u)) =
+              make_uint2(kept_pair(v.x, v.y, n0), kept_pair(v.z, v.w, n1));
+          meta[(r0 + r) * ldm + g_first / 2 + u] = static_cast<uint8_t>(n0 | (n1 << 4));
+          if (Am) {
+            uint4 m;
+            masked_group(v.x, v.y, n0, m.x, m.y);
+            masked_group(v.z, v.w, n1, m.z, m.w);
+            *reinterpret_cast<uint4*>(Am + (r0 + r) * ldam + c0 + 8 * u) = m;
+          }
+        }
+      }
+    } else {
+      const uint32_t bo4 = *reinterpret_cast<const uint32_t*>(&boff[q][u * 4]);
+      const int a0 = static_cast<int>(bo4 & 0xFFu) ^ sw, a1 = static_cast<int>((bo4 >> 8) & 0xFFu) ^ sw;
+      const int a2 = static_cast<int>((bo4 >> 16) & 0xFFu) ^ sw, a3 = static_cast<int>(bo4 >> 24) ^ sw;
+      const uint8_t* p = tile + rt * 128;
+      const uint16_t* tb = &mtab[q][u * 16 * MW];
+      for (int kk = 0; kk < nk; ++kk) {
+        const int r = rt + kk * RSTEP;
+        const bool valid = r < nr && u < uvalid;
+        uint32_t nib = 0x4u;  // a missing group keeps the padding nibble
+        if (valid) {
+          const uint8_t* pr = p + kk * RSTEP * 128;
+          const uint32_t v0 = *reinterpret_cast<const uint16_t*>(pr + a0);
+          const uint32_t v1 = *reinterpret_cast<const uint16_t*>(pr + a1);
+          const uint32_t v2 = *reinterpret_cast<const uint16_t*>(pr + a2);
+          const uint32_t v3 = *reinterpret_cast<const uint16_t*>(pr + a3);
+          const uint32_t lo = v0 | (v1 << 16), hi = v2 | (v3 << 16);
+          nib = pick2_nibble(lo, hi);
+          const uint32_t pair = kept_pair(lo, hi, nib);
+          *reinterpret_cast<uint32_t*>(vals + (r0 + r) * ldv + 2 * (g_first + u)) = pair;
+          if (Am) {
+            uint16_t* dst = Am + (r0 + r) * ldam + c0 + u * M;
+            const uint16_t* sel = tb + nib * MW;
+#pragma unroll
+            for (int c = 0; c < M / 8; ++c) {
+              const uint2 s01 = *reinterpret_cast<const uint2*>(sel + 4 * c);
+              *reinterpret_cast<uint4*>(dst + 8 * c) =
+                  make_uint4(__byte_perm(pair, 0u, s01.x & 0xFFFFu), __byte_perm(pair, 0u, s01.x >> 16),
+                             __byte_perm(pair, 0u, s01.y & 0xFFFFu), __byte_perm(pair, 0u, s01.y >> 16));
+            }
+          }
+        }
+        // groups 2p and 2p+1 are lanes 2p' and 2p'+1 (UR is even, so a lane pair shares a row)
+        const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
+        if (valid && (lane & 1) == 0) {
+          const uint32_t hi_nib = (u + 1 < uvalid) ? other : 0x4u;
+          meta[(r0 + r) * ldm + (g_first + u) / 2] = static_cast<uint8_t>(nib | (hi_nib << 4));
+        }
+      }
+    }
+    // every unit thread is done with buffer q: refill it with item k + 2
+    named_bar_sync(1, kUnitThreads);
+    if (tu == 0 && item + 2 * gridDim.x < n_items) {
+      fence_proxy_async_smem();
+      load(item + 2 * static_cast<int64_t>(gridDim.x), q);
+    }
+  }
+}
+
+// One launch of vnm_prune_swz_kernel<M, CWB> with as many CTAs per SM as fit.
+template <int M, int CWB>
+cudaError_t launch_vnm_prune_swz(const CUtensorMap& tm, int64_t rows, int64_t cols, int V, int sub_bytes,
+                                 int64_t nb, uint8_t* colidx, const p24_sparse& out, uint16_t* am, int64_t ldam,
+                                 int* status, int sms, cudaStream_t s) {
+  constexpr int kThreads = 64 * CWB + 256;
+  const int smem = 2 * CWB * sub_bytes + 1024;  // + the 1024-byte alignment of the swizzled buffers
+  static std::once_flag once[64];
+  static cudaError_t attr[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    attr[dev] = cudaFuncSetAttribute(vnm_prune_swz_kernel<M, CWB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     64 * 1024 + 1024);
+  });
+  if (attr[dev] != cudaSuccess) return attr[dev];
+  static thread_local int occ_smem[64], occ_ctas[64];
+  if (occ_smem[dev] != smem) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vnm_prune_swz_kernel<M, CWB>, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    occ_ctas[dev] = std::max(1, n);
+    occ_smem[dev] = smem;
+  }
+  const int64_t nbx = (cols + 64 * CWB - 1) / (64 * CWB);
+  const int64_t n_items = nb * nbx;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * occ_ctas[dev]));
+  vnm_prune_swz_kernel<M, CWB><<<grid, kThreads, smem, s>>>(tm, rows, cols, V, sub_bytes, n_items, nbx, colidx,
+                                                             static_cast<uint16_t*>(out.vals), out.ldv, out.meta,
+                                                             out.ldm, am, ldam, status);
+  return cudaGetLastError();
+}
+
 // The same prune as a persistent kernel: work item = (row block, CW-column chunk);
 // each item's V x CW tile is brought into shared memory by one TMA box while the
 // previous item is processed (two buffers), so the HBM stream overlaps the serial
@@ -820,6 +1086,48 @@ cudaError_t launch_vnm_compress(const void* A, int64_t rows, int64_t cols, int64
                                 uint8_t* colidx, const p24_sparse& out, void* A_masked, int64_t ldam, cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const int64_t nb = (rows + V - 1) / V;
+  if (V <= 256 && cols % 8 == 0 && M <= 32) {
+    // groups of at most 32 columns: 64-column swizzled boxes (two per item for V <= 128)
+    const int sub_bytes = ((V + 7) / 8) * 1024;
+    CUtensorMap tm;
+    if (!make_tensor_map_2d(&tm, true, A, cols, rows, lda * 2, 64, V, true)) return cudaErrorInvalidValue;
+    int* status = device_status_ptr();
+    if (!status) return cudaErrorInvalidDevice;
+    static std::once_flag once_w[64];
+    static int sms_w[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once_w[dev], [&] {
+      int sms = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      sms_w[dev] = sms > 0 ? sms : 1;
+    });
+    auto* am = static_cast<uint16_t*>(A_masked);
+    const bool two = V <= 128;
+    switch (M) {
+      case 4:
+        e = two ? launch_vnm_prune_swz<4, 2>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s)
+                : launch_vnm_prune_swz<4, 1>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s);
+        break;
+      case 8:
+        e = two ? launch_vnm_prune_swz<8, 2>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s)
+                : launch_vnm_prune_swz<8, 1>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s);
+        break;
+      case 16:
+        e = two ? launch_vnm_prune_swz<16, 2>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s)
+                : launch_vnm_prune_swz<16, 1>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s);
+        break;
+      default:
+        e = two ? launch_vnm_prune_swz<32, 2>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s)
+                : launch_vnm_prune_swz<32, 1>(tm, rows, cols, V, sub_bytes, nb, colidx, out, am, ldam, status, sms_w[dev], s);
+        break;
+    }
+    count_launch();
+    if (e != cudaSuccess) return e;
+    return launch_pad(out, s);
+  }
   if (V <= 256 && cols % 8 == 0 && 2 * V * (M <= 32 ? 64 : 2 * M) * 2 <= 128 * 1024) {
     // persistent, TMA double-buffered: the narrowest chunk that still holds whole
     // metadata bytes (two groups), two buffers of V x CW

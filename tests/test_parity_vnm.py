@@ -38,7 +38,7 @@ def make_a(rows, cols, kind, seed):
 
 # ragged last 256-column chunk, odd group counts, V above the row count, M from 4 to 128
 CASES = [(7, 64, 3, 8), (20, 96, 8, 16), (5, 300, 2, 4), (9, 384, 4, 128), (3, 40, 5, 8), (33, 512, 16, 32),
-         (2, 264, 1, 8), (300, 1024, 64, 8)]
+         (2, 264, 1, 8), (300, 1024, 64, 8), (45, 224, 7, 32), (130, 136, 128, 4), (520, 328, 256, 8)]
 
 
 @pytest.mark.parametrize("rows,cols,V,M", CASES)
@@ -81,7 +81,8 @@ def test_vnm_m4_equals_2to4(P):
 
 
 @pytest.mark.parametrize("rows,cols,V,M", [(300, 1024, 256, 8), (40, 264, 16, 8), (9, 384, 4, 128),
-                                           (600, 512, 300, 8)])
+                                           (600, 512, 300, 8), (520, 328, 256, 8), (77, 96, 32, 16),
+                                           (45, 224, 7, 32), (130, 136, 128, 4), (3, 64, 256, 16)])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_vnm_compress_masked_output(P, rows, cols, V, M, in_place):
     """The dense masked form A_masked (A with every pruned entry +0), written beside the
