@@ -1118,6 +1118,9 @@ int num_sms() {
 // bits while the tile's main loop runs, before the accumulator is ready.
 constexpr int kSpBNWide = 256;
 constexpr int kSpBNOverlap = 192;
+#ifndef P24_OVERLAP_MAX_NKB
+#define P24_OVERLAP_MAX_NKB 0  // K-blocks (of 128) up to which plain epilogues take the overlapped tile
+#endif
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 6;
 
@@ -1152,7 +1155,10 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
                         bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s) {
   if (A.rows == 0 || rowsB == 0) return cudaSuccess;
   const bool heavy_epilogue = epi.act24.vals != nullptr;
-  const int BN = heavy_epilogue ? kSpBNOverlap : kSpBNWide;
+  // Two accumulators (the epilogue of a tile overlaps the next tile's main loop) at the
+  // narrower tile when the epilogue is heavy or the main loop short.
+  const bool overlap = transposed_out && (heavy_epilogue || (A.cols + 127) / 128 <= P24_OVERLAP_MAX_NKB);
+  const int BN = overlap ? kSpBNOverlap : kSpBNWide;
   SpmmParams p{};
   p.rowsA = static_cast<int>(A.rows);
   p.rowsB = static_cast<int>(rowsB);
@@ -1210,9 +1216,11 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
     if (heavy_epilogue) return cudaErrorInvalidValue;  // the activation prune is transposed-only
     return run_spmm<kSpBNWide, false, kEpiStore>(ta, tb, te, tl, tt, p, s);
   }
-  if (heavy_epilogue) return run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
-  if (epi.gate || epi.dbias) return run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
-  return run_spmm<kSpBNWide, true, kEpiStore>(ta, tb, te, tl, tt, p, s);
+  if (heavy_epilogue || epi.gate || epi.dbias)
+    return overlap ? run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, tl, tt, p, s)
+                   : run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
+  return overlap ? run_spmm<kSpBNOverlap, true, kEpiStore>(ta, tb, te, tl, tt, p, s)
+                 : run_spmm<kSpBNWide, true, kEpiStore>(ta, tb, te, tl, tt, p, s);
 }
 
 cudaError_t launch_gemm_nt(const void* A, int64_t M, int64_t lda, const void* B, int64_t N, int64_t ldb, int64_t K,

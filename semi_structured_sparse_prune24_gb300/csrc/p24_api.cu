@@ -112,8 +112,8 @@ void step_layout(int64_t M, int64_t d, int64_t ffn, uint32_t flags, int64_t r, c
   } else {
     L.T_up = L.T_dn = L.U_dn = L.U_up = L.Lt_up = L.Lt_dn = L.Rt_up = L.Rt_dn = nullptr;
   }
-  const int64_t S = colsum_slabs(M);
-  *cs = static_cast<float*>(take(static_cast<size_t>(S * (ffn > d ? ffn : d) * 4)));
+  // db_down's partial sums (colsum_step_slabs(M, d) row slabs of d floats)
+  *cs = static_cast<float*>(take(static_cast<size_t>(colsum_step_slabs(M, d) * d * 4)));
   L.total = off;
 }
 
@@ -613,7 +613,7 @@ int ffn24_step_traced(const p24_ffn_args* a, void* workspace, size_t ws_bytes, v
   });
   // 5. db_down = column sums of dY
   P24_PHASE(5, {
-    if (a->db_down) P24_TRY(cuda_status(launch_colsum(a->dY, M, d, d, a->db_down, cs, s)));
+    if (a->db_down) P24_TRY(cuda_status(launch_colsum_step(a->dY, M, d, d, a->db_down, cs, s)));
   });
   // 6. dW_down = (dY^T H) on mask(W_down)
   P24_PHASE(6, {

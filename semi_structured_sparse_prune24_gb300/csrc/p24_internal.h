@@ -24,6 +24,10 @@ cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s);
 int64_t colsum_slabs(int64_t M);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s);
+// The step's db_down: more row slabs for short inputs; scratch of colsum_step_slabs(M, N) * N floats.
+int64_t colsum_step_slabs(int64_t M, int64_t N);
+cudaError_t launch_colsum_step(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws,
+                               cudaStream_t s);
 // Same sums with the library's fixed device scratch instead of a caller workspace.
 constexpr int64_t kNoAllocColsumScratch = P24_COLSUM_NOALLOC_SCRATCH_FLOATS;  // floats (4 MiB per GPU)
 static_assert(P24_COLSUM_NOALLOC_MAX_COLS <= P24_COLSUM_NOALLOC_SCRATCH_FLOATS,

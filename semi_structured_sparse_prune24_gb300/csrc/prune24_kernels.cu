@@ -947,7 +947,7 @@ __device__ __forceinline__ void add_bf16x8(float* a, const uint4& v) {
 __global__ void __launch_bounds__(256) colsum_partial_kernel(const uint16_t* __restrict__ G, int64_t M, int64_t N,
                                                              int64_t ldg, int64_t rows_per_slab,
                                                              float* __restrict__ part) {
-  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
   if (c0 >= N) return;
   const int64_t s = blockIdx.y;
   const int64_t r0 = s * rows_per_slab;
@@ -980,6 +980,30 @@ __global__ void colsum_final_kernel(const float* __restrict__ part, int64_t S, i
 #pragma unroll 8
   for (int64_t s = 0; s < S; ++s) a += part[s * N + col];
   out[col] = a;
+}
+
+// The S partial sums of 32 columns per CTA: warp w adds slabs [w S/8, (w+1) S/8) in
+// order, then the 8 warp sums are added in warp order (a fixed order for given S).
+__global__ void __launch_bounds__(256) colsum_final_wide_kernel(const float* __restrict__ part, int64_t S,
+                                                                int64_t N, float* __restrict__ out) {
+  __shared__ float ws[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const int64_t per = (S + 7) / 8;
+  const int64_t s0 = warp * per, s1 = min(S, s0 + per);
+  float a = 0.f;
+  if (col < N) {
+#pragma unroll 8
+    for (int64_t sl = s0; sl < s1; ++sl) a += part[sl * N + col];
+  }
+  ws[warp][lane] = a;
+  __syncthreads();
+  if (warp == 0 && col < N) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += ws[w][lane];
+    out[col] = t;
+  }
 }
 
 // Scratch of p24_colsum_noalloc: a fixed device array, so that the call needs
@@ -1257,6 +1281,35 @@ cudaError_t launch_colsum_noalloc(const void* G, int64_t M, int64_t N, int64_t l
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   colsum_final_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(ws, S, N, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// The training step's db_down: as many row slabs as keep about 8 CTAs per SM busy
+// (each CTA a slab of at least 16 rows x up to 2048 columns), so that short, wide
+// and narrow inputs alike have enough loads in flight; then the parallel final sum.
+int64_t colsum_step_slabs(int64_t M, int64_t N) {
+  const int64_t ncb = (N + 2047) / 2048;
+  int64_t S = (1216 + ncb - 1) / ncb;
+  S = std::min<int64_t>(S, (M + 15) / 16);
+  S = std::min<int64_t>(S, 1024);
+  return std::max<int64_t>(S, 1);
+}
+
+cudaError_t launch_colsum_step(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws,
+                               cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  if (M == 0) return cudaMemsetAsync(out, 0, N * sizeof(float), s);
+  const int64_t S = colsum_step_slabs(M, N);
+  const int64_t rps = (M + S - 1) / S;
+  const int64_t cols_per_cta = std::min<int64_t>(2048, (N + 7) / 8 * 8);
+  const int threads = static_cast<int>(((cols_per_cta / 8) + 31) / 32 * 32);
+  dim3 grid(static_cast<unsigned>((N + cols_per_cta - 1) / cols_per_cta), static_cast<unsigned>(S));
+  colsum_partial_kernel<<<grid, threads, 0, s>>>(static_cast<const uint16_t*>(G), M, N, ldg, rps, ws);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colsum_final_wide_kernel<<<static_cast<unsigned>((N + 31) / 32), 256, 0, s>>>(ws, S, N, out);
   count_launch();
   return cudaGetLastError();
 }
