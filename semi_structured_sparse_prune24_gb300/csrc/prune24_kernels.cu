@@ -56,6 +56,21 @@ __device__ __forceinline__ uint32_t pick2_code(uint32_t lo, uint32_t hi) {
   return ((top & 3u) << 2) | (second & 3u);
 }
 
+// pick2_code with the upper halves taken by a multiply-high (hi16 = 2^16, passed at
+// run time so that it stays a multiply): the shift moves from the integer pipe to the
+// FMA pipe, which the prune kernels leave mostly idle.
+__device__ __forceinline__ uint32_t pick2_code_mh(uint32_t lo, uint32_t hi, uint32_t hi16) {
+  const uint32_t c0 = lo * 131072u + 3u;
+  const uint32_t c1 = __umulhi(lo, hi16) * 131072u + 2u;
+  const uint32_t c2 = hi * 131072u + 1u;
+  const uint32_t c3 = __umulhi(hi, hi16) * 131072u;
+  const uint32_t a = max(c0, c1), b = min(c0, c1);
+  const uint32_t c = max(c2, c3), d = min(c2, c3);
+  const uint32_t top = max(a, c);
+  const uint32_t second = max(min(a, c), max(b, d));
+  return ((top & 3u) << 2) | (second & 3u);
+}
+
 // Row of the pick table for code t (unused codes, where both positions agree, are 0):
 //   x = byte selector of the kept pair from (lo, hi) | nibble << 16
 //   y = selector keeping lo's kept halves (others from a zero word) | the same for hi << 16
@@ -736,6 +751,7 @@ struct DpArgs {
   int64_t ldtm;
   uint16_t* Wm;             // optional dense forward-masked copy: [rows, ldwm], or with
   int64_t ldwm;             // kMaskedT its transpose [cols, ldwm]
+  uint32_t hi16;            // 2^16 (see pick2_code_mh)
 };
 
 // One 128 x 128 tile. kEdge: the tile crosses the last row or column, so every
@@ -784,13 +800,13 @@ __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t c
       const bool full = !kEdge || (row < p.rows && e + 8 <= p.cols);
       const bool half = kEdge && row < p.rows && !full && e + 4 <= p.cols;
       if (full || half) {
-        const uint2 r0 = ptab[pick2_code(v[i].x, v[i].y)];
+        const uint2 r0 = ptab[pick2_code_mh(v[i].x, v[i].y, p.hi16)];
         const uint32_t n0 = r0.x >> 16;
         const uint32_t k0 = __byte_perm(v[i].x, v[i].y, r0.x);
         v[i].x = __byte_perm(v[i].x, 0u, r0.y);
         v[i].y = __byte_perm(v[i].y, 0u, r0.y >> 16);
         if (full) {
-          const uint2 r1 = ptab[pick2_code(v[i].z, v[i].w)];
+          const uint2 r1 = ptab[pick2_code_mh(v[i].z, v[i].w, p.hi16)];
           const uint32_t n1 = r1.x >> 16;
           const uint32_t k1 = __byte_perm(v[i].z, v[i].w, r1.x);
           v[i].z = __byte_perm(v[i].z, 0u, r1.y);
@@ -836,7 +852,7 @@ __device__ __forceinline__ void dp_tile(const DpArgs& p, int64_t row0, int64_t c
       const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
       const uint32_t lo = __byte_perm(w0[j >> 1], w1[j >> 1], sel);
       const uint32_t hi = __byte_perm(w2[j >> 1], w3[j >> 1], sel);
-      const uint32_t entry = ptab[pick2_code(lo, hi)].x;
+      const uint32_t entry = ptab[pick2_code_mh(lo, hi, p.hi16)].x;
       const uint32_t nib = entry >> 16;
       const uint32_t pair = __byte_perm(lo, hi, entry);
       const uint32_t nib_next = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
@@ -1098,7 +1114,7 @@ cudaError_t launch_compress_both(const void* W, int64_t rows, int64_t cols, int6
   if (W_masked && W_masked_T) return cudaErrorInvalidValue;
   const DpArgs a{w,       ldw,  nullptr, static_cast<uint16_t*>(fwd.vals), fwd.ldv, nullptr, fwd.meta, fwd.ldm,
                  rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm,
-                 static_cast<uint16_t*>(W_masked_T ? W_masked_T : W_masked), W_masked_T ? ldwmT : ldwm};
+                 static_cast<uint16_t*>(W_masked_T ? W_masked_T : W_masked), W_masked_T ? ldwmT : ldwm, 65536u};
   cudaError_t e = W_masked_T ? launch_double_prune<true, false, true>(a, s)
                              : (W_masked ? launch_double_prune<true, true>(a, s) : launch_double_prune<true, false>(a, s));
   if (e != cudaSuccess) return e;
@@ -1228,7 +1244,7 @@ cudaError_t launch_transpose_repack(const p24_sparse& fwd, const p24_sparse& bwd
   if (rows == 0 || cols == 0) return cudaSuccess;
   const DpArgs a{nullptr, 0,    static_cast<const uint16_t*>(fwd.vals), nullptr, fwd.ldv, fwd.meta, nullptr, fwd.ldm,
                  rows,    cols, static_cast<uint16_t*>(bwdT.vals), bwdT.ldv, bwdT.meta, bwdT.ldm,
-                 static_cast<uint16_t*>(W_masked_T), ldwmT};
+                 static_cast<uint16_t*>(W_masked_T), ldwmT, 65536u};
   const cudaError_t e = W_masked_T ? launch_double_prune<false, false, true>(a, s) : launch_double_prune<false, false>(a, s);
   if (e != cudaSuccess) return e;
   return launch_pad(bwdT, s);
