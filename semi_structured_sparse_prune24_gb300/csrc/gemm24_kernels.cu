@@ -792,7 +792,10 @@ struct DwSmem {
   // spare bytes after the last B stage: a B descriptor covers this CTA's 128
   // columns, and the pad keeps even a read of the full 256 inside the allocation
   static constexpr int kPad = 2 * 8192;
-  static constexpr int kOffBar = kOffB + STAGES * kB + kPad;
+  // epilogue staging: per epilogue warp 32 dW rows x 64 columns of bf16 (4 KB)
+  static constexpr int kOffStage = kOffB + STAGES * kB + kPad;
+  static constexpr int kStage = 32 * 64 * 2;
+  static constexpr int kOffBar = kOffStage + 4 * kStage;
   static constexpr int kBytes = kOffBar + 8 * (2 * STAGES + 5) + 16;
   static constexpr int kTxPair = 2 * (kA + kB);  // both CTAs' A and B, counted on the leader's barrier
 };
@@ -930,6 +933,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const bool extra = ta >= p.tilesA_main || tb >= p.tilesB_main;
       const int b = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
+      // The mask bytes of this thread's dW row in the tile (8 columns a byte), read
+      // while the tile's main loop still runs, so that no load sits in the epilogue.
+      uint32_t mwc[BN / 32] = {};
+      if constexpr (kMasked) {
+        if (!extra) {
+          const int n = (2 * ta + rank) * kBM + q * 32 + lane;
+          const int kb0 = tb * BN / 8;  // first mask byte of the tile
+          if (n < p.N) {
+            const uint8_t* mrow = p.meta + static_cast<int64_t>(n) * p.ldm + kb0;
+            if (kb0 + BN / 8 <= p.ldm) {
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h) {
+                const uint4 x = *reinterpret_cast<const uint4*>(mrow + 16 * h);
+                mwc[4 * h] = x.x;
+                mwc[4 * h + 1] = x.y;
+                mwc[4 * h + 2] = x.z;
+                mwc[4 * h + 3] = x.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 8; ++i)
+                if (kb0 + i < p.ldm) mwc[i / 4] |= static_cast<uint32_t>(mrow[i]) << (8 * (i % 4));
+            }
+          }
+        }
+      }
       if (!p24_wait(&acc_full[b], aph, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t acc = tmem + b * BN + (static_cast<uint32_t>(q * 32) << 16);
@@ -960,21 +989,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         continue;
       }
       ta = 2 * ta + rank;
-      const int n = ta * kBM + q * 32 + lane;  // row of dW
-      const bool row_ok = n < p.N;
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32_wait(acc + c * 32, v);
-        const int k0 = tb * BN + c * 32;
-        if (row_ok && k0 < p.K) {
+      // Thread = dW row ta * kBM + q * 32 + lane (its TMEM lane). Two 32-column chunks of
+      // the warp's 32 rows go through a 32 x 64 shared-memory stage (16-byte pieces
+      // XOR-swizzled by row: the row writes and the line reads are both free of bank
+      // conflicts), so that each store instruction writes 4 rows x 128 bytes.
+      const int row0 = ta * kBM + q * 32;
+      uint8_t* stg = smem + L::kOffStage + q * L::kStage;
+      for (int cp = 0; cp < BN / 64; ++cp) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * cp + h;
+          uint32_t v[32];
+          tc_ld_32x32b_x32_wait(acc + c * 32, v);
           uint32_t w[16];
           if constexpr (kMasked) {
-            const int nbytes = min(4, (p.K - k0) / 8);  // 8 columns per metadata byte
-            uint32_t mw = 0;
-            const uint8_t* mrow = p.meta + static_cast<int64_t>(n) * p.ldm + k0 / 8;
-            if (nbytes == 4) mw = *reinterpret_cast<const uint32_t*>(mrow);
-            else
-              for (int i = 0; i < nbytes; ++i) mw |= static_cast<uint32_t>(mrow[i]) << (8 * i);
+            // bytes past the last column are padding (0x44) or unread: their groups are
+            // past K, so no store reads them
+            uint32_t mw = mwc[0];  // mwc[c] by selects: the words stay in registers
+#pragma unroll
+            for (int i = 1; i < BN / 32; ++i) mw = (c == i) ? mwc[i] : mw;
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
               const uint32_t nib = (mw >> (4 * g)) & 0xFu;
@@ -989,13 +1022,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
             for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
           }
-          __nv_bfloat16* o = p.out + static_cast<int64_t>(n) * p.ldo + k0;
 #pragma unroll
           for (int pc = 0; pc < 4; ++pc)
-            if (k0 + pc * 8 < p.K)
-              *reinterpret_cast<uint4*>(o + pc * 8) =
-                  make_uint4(w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+            *reinterpret_cast<uint4*>(stg + lane * 128 + (((4 * h + pc) ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
         }
+        __syncwarp();
+        const int kc = tb * BN + cp * 64 + (lane & 7) * 8;  // this lane's 8 columns
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int row = 4 * r + (lane >> 3);
+          const uint4 x = *reinterpret_cast<const uint4*>(stg + row * 128 + (((lane & 7) ^ (row & 7)) << 4));
+          if (row0 + row < p.N && kc < p.K)
+            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row0 + row) * p.ldo + kc) = x;
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
