@@ -271,8 +271,16 @@ enum SpmmEpi : int {
   kEpiFull = 1,   // any of: ReLU' gate, 2:4 activation prune, column sums (transposed output)
 };
 
+// Threads that gather B rows in the V:2:M mode (a multiple of 64, at most 512; measured
+// on the 70B down GEMM: 128 -> 256 -> 512 threads gave 2.26 -> 2.06 -> 1.93 ms at M = 16384).
+#ifndef P24_GATHER_THREADS
+#define P24_GATHER_THREADS 512
+#endif
+constexpr int kGatherThreads = P24_GATHER_THREADS;
+static_assert(kGatherThreads % 64 == 0 && kGatherThreads <= 512, "gather threads");
+
 template <int BN, int STAGES, bool kTransOut, int kEpi, bool kGather = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 448 : 320, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGatherThreads : 320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmL,
                 const __grid_constant__ CUtensorMap tmT, const SpmmParams p) {
@@ -312,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 448 : 320,
       mbar_init(&full[s], kGather ? 2 : 1);
       mbar_init(&empty[s], 1);
       mbar_init(&meta_ready[s], 8);  // 4 mover warps x 2 CTAs
-      if (kGather) mbar_init(&bfull[s], 128);  // one arrival per gather thread
+      if (kGather) mbar_init(&bfull[s], kGatherThreads);  // one arrival per gather thread
     }
     for (int e = 0; e < kEBufs; ++e) {
       mbar_init(&efull[e], 1);
@@ -351,14 +359,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 448 : 320,
     // ------------------------------------------------ gather warps (both CTAs, gathered B)
     // Stage rows (128 condensed K = 32 groups of 4 selected rows of M) are copied as 16
     // pieces of 16 bytes (this CTA's 128 columns): thread th takes piece c = th % 16 of
-    // rows r = 8 i + th / 16, i < 16, so a half warp reads one row's 256 bytes. Row r is
-    // row (32 kb + r / 4) M + colidx byte r % 4 of B; its piece c lands in atom c / 8,
-    // chunk (c % 8) ^ (r % 8) of the 128B-swizzled MN-major layout. Each thread then
-    // arrives once on bfull[s] when its copies have landed.
+    // rows r = RS i + th / 16 (RS = gather threads / 16, i < 128 / RS), so a half warp
+    // reads one row's 256 bytes. Row r is row (32 kb + r / 4) M + colidx byte r % 4 of B;
+    // its piece c lands in atom c / 8, chunk (c % 8) ^ (r % 8) of the 128B-swizzled
+    // MN-major layout. Each thread then arrives once on bfull[s] when its copies have landed.
+    constexpr int RS = kGatherThreads / 16;  // rows between a thread's rows
+    constexpr int NR = 128 / RS;             // rows per thread per stage
     const int th = threadIdx.x - 320;
     const int c = th & 15;
     const uint32_t sh = 8u * static_cast<uint32_t>((th >> 4) & 3);  // colidx byte of this thread's rows
-    const int gofs = th >> 6;                                       // its rows' group within a pair of groups
+    const int gofs = th >> 6;                                       // its first row's group
     uint32_t it = 0;
     bool ok = true;
     for (int t = cid; t < p.num_tiles && ok; t += ncl) {
@@ -367,9 +377,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 448 : 320,
       const uint32_t* cix = p.vnm_cix + static_cast<int64_t>((ta * 2 * kBM) / p.vnm_V) * p.vnm_G + gofs;
       const uint16_t* bsrc = p.vnm_B + tb * BN + rank * (BN / 2) + 8 * c;
       const uint32_t dst0 = smem_u32(smem + L::kOffB) + (c >> 3) * 16384u;
-      uint32_t cw[16];  // colidx words of this thread's 16 rows for the current stage
+      uint32_t cw[NR];  // colidx words of this thread's rows for the current stage
 #pragma unroll
-      for (int i = 0; i < 16; ++i) cw[i] = __ldg(cix + 2 * i);
+      for (int i = 0; i < NR; ++i) cw[i] = __ldg(cix + (RS / 4) * i);
       for (int kb = 0; kb < p.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
@@ -377,16 +387,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 448 : 320,
         const uint32_t dst = dst0 + static_cast<uint32_t>(s * L::kB);
         const int gb = kb * 32 + gofs;  // every stage is full: the host requires 128 | condensed K
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = 8 * i + (th >> 4);
-          const int y = (gb + 2 * i) * p.vnm_group + static_cast<int>((cw[i] >> sh) & 0xFFu);
+        for (int i = 0; i < NR; ++i) {
+          const int r = RS * i + (th >> 4);
+          const int y = (gb + (RS / 4) * i) * p.vnm_group + static_cast<int>((cw[i] >> sh) & 0xFFu);
           cp_async_16(dst + static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(c & 7) ^ static_cast<uint32_t>(r & 7)) << 4),
                       bsrc + static_cast<int64_t>(y) * p.vnm_ldb);
         }
         cp_async_arrive(&bfull[s]);
         if (kb + 1 < p.nkb) {  // the next stage's words, loaded while this stage's copies fly
 #pragma unroll
-          for (int i = 0; i < 16; ++i) cw[i] = __ldg(cix + (kb + 1) * 32 + 2 * i);
+          for (int i = 0; i < NR; ++i) cw[i] = __ldg(cix + (kb + 1) * 32 + (RS / 4) * i);
         }
       }
     }
@@ -1146,7 +1156,7 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   using L = SpmmSmem<BN, kSpStages>;
   auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi, kGather>;
   const int smem = L::kBytes + 1024;
-  constexpr int kThreads = kGather ? 448 : 320;  // + 4 gather warps
+  constexpr int kThreads = kGather ? 320 + kGatherThreads : 320;  // + the gather warps
   static LaunchSetup setup;
   int clusters = 0;
   cudaError_t err = launch_setup(setup, kern, 2, kThreads, smem, clusters);
