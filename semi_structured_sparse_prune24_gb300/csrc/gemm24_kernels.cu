@@ -622,19 +622,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
         // The ReLU' gate of this warp's 32 features, one word per token (bit l:
         // gate(m, n_warp + l) > 0), read from the bf16 gate while the tile's main
         // loop still runs, so that no load sits in the epilogue's critical path.
-        for (int j = lane; j < BN; j += 32) {
-          const int m = tb * BN + j;
-          uint32_t word = 0;
-          if (m < p.rowsB) {
+        // Four tokens per lane at a time: their 16 loads are all issued before any is used.
+        for (int j0 = lane; j0 < BN; j0 += 128) {
+          uint4 x[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u;
+            const int m = tb * BN + j;
+            const bool row_in = j < BN && m < p.rowsB;
             const uint16_t* g = p.gate + static_cast<int64_t>(m) * p.ldg + n_warp;
-            uint4 x[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              x[k] = n_warp + 8 * k < p.rowsA ? *reinterpret_cast<const uint4*>(g + 8 * k) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) word |= positive_bits(x[k]) << (8 * k);
+              x[u][k] = row_in && n_warp + 8 * k < p.rowsA ? __ldg(reinterpret_cast<const uint4*>(g + 8 * k))
+                                                          : make_uint4(0, 0, 0, 0);
           }
-          gstage[j] = word;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u;
+            uint32_t word = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) word |= positive_bits(x[u][k]) << (8 * k);
+            if (j < BN) gstage[j] = word;
+          }
         }
         __syncwarp();
       }
