@@ -354,6 +354,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  pdl_wait();  // the previous kernel's outputs (under programmatic launch)
+  pdl_trigger();
 
   if (kGather && warp >= 10) {
     // ------------------------------------------------ gather warps (both CTAs, gathered B)
@@ -843,6 +845,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  pdl_wait();  // the previous kernel's outputs (under programmatic launch)
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
@@ -1172,7 +1176,8 @@ cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorM
   if (err != cudaSuccess) return err;
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
-  kern<<<grid, kThreads, smem, s>>>(a, b, e, l, t, p);
+  err = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a, b, e, l, t, p);
+  if (err != cudaSuccess) return err;
   count_launch();
   return cudaGetLastError();
 }
@@ -1405,7 +1410,8 @@ cudaError_t run_dw(const void* dY, int64_t lddy, const void* X, int64_t ldx, int
   if (err != cudaSuccess) return err;
   if (clusters == 0) clusters = num_sms() / 2;
   const int grid = 2 * std::min(p.num_tiles, clusters);  // clusters of 2, all resident
-  kern<<<grid, 192, smem, s>>>(ta, tb, ta2, tb2, p);
+  err = launch_pdl(kern, dim3(grid), dim3(192), smem, s, ta, tb, ta2, tb2, p);
+  if (err != cudaSuccess) return err;
   count_launch();
   return cudaGetLastError();
 }

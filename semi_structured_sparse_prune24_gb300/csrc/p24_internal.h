@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -107,6 +108,39 @@ bool make_tensor_map_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t in
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128 = false);
 
 int* device_status_ptr();  // the status word of the current device
+
+// Launch with programmatic stream serialization: the kernel may start while the
+// stream's previous kernel finishes, and must call pdl_wait() before touching global
+// memory (p24_ptx.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// The same launch without the attribute (stream order as usual). Measured: the fused
+// prune + double prune is faster launched this way (the 70B tail step 2.03 -> 1.97 ms
+// against programmatic launch), while the GEMMs and column sums gain from it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                         Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Count one kernel launch (called by every launcher after a successful launch).
 void count_launch();

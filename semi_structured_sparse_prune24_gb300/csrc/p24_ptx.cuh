@@ -27,6 +27,17 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the previous
+// kernel of the stream still runs. pdl_wait blocks until that kernel has completed and
+// its memory operations are visible: every such kernel calls it after its purely local
+// setup (barriers, TMEM, shared tables) and before its first global memory access.
+// pdl_trigger lets the next kernel launch once every CTA of this one has called it (so
+// all of this kernel's CTAs are already resident when a dependent CTA can take an SM).
+// Both are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -418,6 +418,8 @@ __global__ void __launch_bounds__(64 * CWB + 256) vnm_prune_swz_kernel(
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   if (t == 0) {
     load(blockIdx.x, 0);
     if (blockIdx.x + gridDim.x < n_items) load(blockIdx.x + gridDim.x, 1);
@@ -616,10 +618,9 @@ cudaError_t launch_vnm_prune_swz(const CUtensorMap& tm, int64_t rows, int64_t co
   const int64_t nbx = (cols + 64 * CWB - 1) / (64 * CWB);
   const int64_t n_items = nb * nbx;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * occ_ctas[dev]));
-  vnm_prune_swz_kernel<M, CWB><<<grid, kThreads, smem, s>>>(tm, rows, cols, V, sub_bytes, n_items, nbx, colidx,
-                                                             static_cast<uint16_t*>(out.vals), out.ldv, out.meta,
-                                                             out.ldm, am, ldam, status);
-  return cudaGetLastError();
+  return launch_pdl(vnm_prune_swz_kernel<M, CWB>, dim3(grid), dim3(kThreads), smem, s, tm, rows, cols, V, sub_bytes,
+                    n_items, nbx, colidx, static_cast<uint16_t*>(out.vals), out.ldv, out.meta, out.ldm, am, ldam,
+                    status);
 }
 
 // The same prune as a persistent kernel: work item = (row block, CW-column chunk);
@@ -887,6 +888,8 @@ __global__ void __launch_bounds__(256, 4) double_prune_interior_kernel(const DpA
   __shared__ uint2 ptab[16];
   if (threadIdx.x < 16) ptab[threadIdx.x] = pick_row(threadIdx.x);
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kDpCols;
   for (int64_t row0 = static_cast<int64_t>(blockIdx.y) * kDpRows; row0 < rows_full;
        row0 += static_cast<int64_t>(gridDim.y) * kDpRows)
@@ -900,6 +903,8 @@ __global__ void __launch_bounds__(256, 2) double_prune_border_kernel(const DpArg
   __shared__ uint2 ptab[16];
   if (threadIdx.x < 16) ptab[threadIdx.x] = pick_row(threadIdx.x);
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   const int64_t bx = t < n_col_part ? full_bx : t - n_col_part;
   const int64_t by = t < n_col_part ? t : full_by;
@@ -914,14 +919,18 @@ cudaError_t launch_double_prune(const DpArgs& a, cudaStream_t s) {
   const int64_t nby = (a.rows + kDpRows - 1) / kDpRows;
   if (full_bx > 0 && full_by > 0) {
     dim3 grid(static_cast<unsigned>(full_bx), grid_y(full_by));
-    double_prune_interior_kernel<kFromDense, kMasked, kMaskedT><<<grid, 256, 0, s>>>(a, full_by * kDpRows);
+    const cudaError_t e = launch_plain(double_prune_interior_kernel<kFromDense, kMasked, kMaskedT>, grid, dim3(256), 0,
+                                     s, a, full_by * kDpRows);
+    if (e != cudaSuccess) return e;
     count_launch();
   }
   const int64_t n_col_part = (a.cols % kDpCols) ? nby : 0;       // last block column, every block row
   const int64_t n_row_part = (a.rows % kDpRows) ? full_bx : 0;   // last block row, full block columns
   if (n_col_part + n_row_part > 0) {
-    double_prune_border_kernel<kFromDense, kMasked, kMaskedT>
-        <<<static_cast<unsigned>(n_col_part + n_row_part), 256, 0, s>>>(a, n_col_part, full_bx, full_by);
+    const cudaError_t e = launch_plain(double_prune_border_kernel<kFromDense, kMasked, kMaskedT>,
+                                     dim3(static_cast<unsigned>(n_col_part + n_row_part)), dim3(256), 0, s, a,
+                                     n_col_part, full_bx, full_by);
+    if (e != cudaSuccess) return e;
     count_launch();
   }
   return cudaGetLastError();
@@ -931,6 +940,8 @@ cudaError_t launch_double_prune(const DpArgs& a, cudaStream_t s) {
 // Zero values past cols/2 and 0x4 nibbles past the last group, up to the strides.
 __global__ void pad_kernel(uint16_t* __restrict__ vals, int64_t ldv, uint8_t* __restrict__ meta, int64_t ldm,
                            int64_t rows, int64_t cols) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nv = ldv - cols / 2;
   const int64_t groups = cols / 4;
   const int64_t mb0 = (groups + 1) / 2;  // first byte with no data nibble
@@ -963,6 +974,8 @@ __device__ __forceinline__ void add_bf16x8(float* a, const uint4& v) {
 __global__ void __launch_bounds__(256) colsum_partial_kernel(const uint16_t* __restrict__ G, int64_t M, int64_t N,
                                                              int64_t ldg, int64_t rows_per_slab,
                                                              float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
   if (c0 >= N) return;
   const int64_t s = blockIdx.y;
@@ -1003,6 +1016,8 @@ __global__ void colsum_final_kernel(const float* __restrict__ part, int64_t S, i
 __global__ void __launch_bounds__(256) colsum_final_wide_kernel(const float* __restrict__ part, int64_t S,
                                                                 int64_t N, float* __restrict__ out) {
   __shared__ float ws[8][32];
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   const int64_t per = (S + 7) / 8;
@@ -1081,10 +1096,10 @@ cudaError_t launch_pad(const p24_sparse& d, cudaStream_t s) {
   if (per_row <= 0 || d.rows == 0) return cudaSuccess;
   const int64_t total = d.rows * per_row;
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 16);
-  pad_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<uint16_t*>(d.vals), d.ldv, d.meta, d.ldm,
-                                                           d.rows, d.cols);
+  const cudaError_t e = launch_pdl(pad_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                                   static_cast<uint16_t*>(d.vals), d.ldv, d.meta, d.ldm, d.rows, d.cols);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_compress(const void* W, int64_t rows, int64_t cols, int64_t ldw, const p24_sparse& out,
@@ -1321,13 +1336,14 @@ cudaError_t launch_colsum_step(const void* G, int64_t M, int64_t N, int64_t ldg,
   const int64_t cols_per_cta = std::min<int64_t>(2048, (N + 7) / 8 * 8);
   const int threads = static_cast<int>(((cols_per_cta / 8) + 31) / 32 * 32);
   dim3 grid(static_cast<unsigned>((N + cols_per_cta - 1) / cols_per_cta), static_cast<unsigned>(S));
-  colsum_partial_kernel<<<grid, threads, 0, s>>>(static_cast<const uint16_t*>(G), M, N, ldg, rps, ws);
+  cudaError_t e = launch_pdl(colsum_partial_kernel, grid, dim3(threads), 0, s, static_cast<const uint16_t*>(G), M, N,
+                             ldg, rps, ws);
   count_launch();
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  colsum_final_wide_kernel<<<static_cast<unsigned>((N + 31) / 32), 256, 0, s>>>(ws, S, N, out);
+  e = launch_pdl(colsum_final_wide_kernel, dim3(static_cast<unsigned>((N + 31) / 32)), dim3(256), 0, s,
+                 static_cast<const float*>(ws), S, N, out);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_colsum(const void* G, int64_t M, int64_t N, int64_t ldg, float* out, float* ws, cudaStream_t s) {
