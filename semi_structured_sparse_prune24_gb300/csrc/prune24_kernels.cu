@@ -546,37 +546,49 @@ __global__ void __launch_bounds__(64 * CWB + 256) vnm_prune_swz_kernel(
       const int a2 = static_cast<int>((bo4 >> 16) & 0xFFu) ^ sw, a3 = static_cast<int>(bo4 >> 24) ^ sw;
       const uint8_t* p = tile + rt * 128;
       const uint16_t* tb = &mtab[q][u * 16 * MW];
-      for (int kk = 0; kk < nk; ++kk) {
-        const int r = rt + kk * RSTEP;
-        const bool valid = r < nr && u < uvalid;
-        uint32_t nib = 0x4u;  // a missing group keeps the padding nibble
-        if (valid) {
-          const uint8_t* pr = p + kk * RSTEP * 128;
-          const uint32_t v0 = *reinterpret_cast<const uint16_t*>(pr + a0);
-          const uint32_t v1 = *reinterpret_cast<const uint16_t*>(pr + a1);
-          const uint32_t v2 = *reinterpret_cast<const uint16_t*>(pr + a2);
-          const uint32_t v3 = *reinterpret_cast<const uint16_t*>(pr + a3);
-          const uint32_t lo = v0 | (v1 << 16), hi = v2 | (v3 << 16);
-          nib = pick2_nibble(lo, hi);
-          const uint32_t pair = kept_pair(lo, hi, nib);
-          *reinterpret_cast<uint32_t*>(vals + (r0 + r) * ldv + 2 * (g_first + u)) = pair;
-          if (Am) {
-            uint16_t* dst = Am + (r0 + r) * ldam + c0 + u * M;
-            const uint16_t* sel = tb + nib * MW;
+      // two rows (RSTEP apart) per iteration: their 8 loads are issued before either is used
+      for (int kk = 0; kk < nk; kk += 2) {
+        uint32_t v[2][4];
+        bool valid[2];
 #pragma unroll
-            for (int c = 0; c < M / 8; ++c) {
-              const uint2 s01 = *reinterpret_cast<const uint2*>(sel + 4 * c);
-              *reinterpret_cast<uint4*>(dst + 8 * c) =
-                  make_uint4(__byte_perm(pair, 0u, s01.x & 0xFFFFu), __byte_perm(pair, 0u, s01.x >> 16),
-                             __byte_perm(pair, 0u, s01.y & 0xFFFFu), __byte_perm(pair, 0u, s01.y >> 16));
-            }
+        for (int h = 0; h < 2; ++h) {
+          const int r = rt + (kk + h) * RSTEP;
+          valid[h] = kk + h < nk && r < nr && u < uvalid;
+          if (valid[h]) {
+            const uint8_t* pr = p + (kk + h) * RSTEP * 128;
+            v[h][0] = *reinterpret_cast<const uint16_t*>(pr + a0);
+            v[h][1] = *reinterpret_cast<const uint16_t*>(pr + a1);
+            v[h][2] = *reinterpret_cast<const uint16_t*>(pr + a2);
+            v[h][3] = *reinterpret_cast<const uint16_t*>(pr + a3);
           }
         }
-        // groups 2p and 2p+1 are lanes 2p' and 2p'+1 (UR is even, so a lane pair shares a row)
-        const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
-        if (valid && (lane & 1) == 0) {
-          const uint32_t hi_nib = (u + 1 < uvalid) ? other : 0x4u;
-          meta[(r0 + r) * ldm + (g_first + u) / 2] = static_cast<uint8_t>(nib | (hi_nib << 4));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = rt + (kk + h) * RSTEP;
+          uint32_t nib = 0x4u;  // a missing group keeps the padding nibble
+          if (valid[h]) {
+            const uint32_t lo = v[h][0] | (v[h][1] << 16), hi = v[h][2] | (v[h][3] << 16);
+            nib = pick2_nibble(lo, hi);
+            const uint32_t pair = kept_pair(lo, hi, nib);
+            *reinterpret_cast<uint32_t*>(vals + (r0 + r) * ldv + 2 * (g_first + u)) = pair;
+            if (Am) {
+              uint16_t* dst = Am + (r0 + r) * ldam + c0 + u * M;
+              const uint16_t* sel = tb + nib * MW;
+#pragma unroll
+              for (int c = 0; c < M / 8; ++c) {
+                const uint2 s01 = *reinterpret_cast<const uint2*>(sel + 4 * c);
+                *reinterpret_cast<uint4*>(dst + 8 * c) =
+                    make_uint4(__byte_perm(pair, 0u, s01.x & 0xFFFFu), __byte_perm(pair, 0u, s01.x >> 16),
+                               __byte_perm(pair, 0u, s01.y & 0xFFFFu), __byte_perm(pair, 0u, s01.y >> 16));
+              }
+            }
+          }
+          // groups 2p and 2p+1 are lanes 2p' and 2p'+1 (UR is even, so a lane pair shares a row)
+          const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, nib, 1);
+          if (valid[h] && (lane & 1) == 0) {
+            const uint32_t hi_nib = (u + 1 < uvalid) ? other : 0x4u;
+            meta[(r0 + r) * ldm + (g_first + u) / 2] = static_cast<uint8_t>(nib | (hi_nib << 4));
+          }
         }
       }
     }
