@@ -298,7 +298,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
   const int nstages = p.nkb + p.nad;  // per tile: sparse stages, then dense ones
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps shared (not generic) accesses
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // leader's is used
   uint64_t* empty = full + STAGES;                                    // leader's commit, both CTAs
   uint64_t* meta_ready = empty + STAGES;                              // leader's is used (8 arrivals)
@@ -804,7 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   constexpr int BN = 256;
   constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, false, /*a_mn=*/true, /*b_mn=*/true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // keeps shared (not generic) accesses
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // leader's is used
   uint64_t* empty = full + STAGES;                                    // leader's commit, both CTAs
   uint64_t* acc_full = empty + STAGES;                                // [2] leader's commit, both CTAs

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(256) vnm_compress_staged_kernel(
 //   with item k + 2. Stage k & 1 is rewritten only for item k + 2, whose tile cannot
 //   arrive before that point, so the stages need no barrier of their own.
 template <int M, int CWB>
-__global__ void __launch_bounds__(64 * CWB + 256) vnm_prune_swz_kernel(
+__global__ void __launch_bounds__(64 * CWB + 256, 3) vnm_prune_swz_kernel(
     const __grid_constant__ CUtensorMap tmA, int64_t rows, int64_t cols, int V, int sub_bytes, int64_t n_items,
     int64_t nbx, uint8_t* __restrict__ colidx, uint16_t* __restrict__ vals, int64_t ldv,
     uint8_t* __restrict__ meta, int64_t ldm, uint16_t* Am, int64_t ldam, int* status) {
@@ -399,7 +399,9 @@ __global__ void __launch_bounds__(64 * CWB + 256) vnm_prune_swz_kernel(
   __shared__ __align__(16) uint16_t mtab[2][M == 4 ? 8 : 512 * CWB];  // [stage][group][nibble][word]
   __shared__ __align__(8) uint64_t full[2];
   __shared__ __align__(8) uint64_t sel_full[2];
-  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned (the 128B swizzle), offset from the shared-memory pointer itself so
+  // that the compiler keeps shared-memory (not generic) loads
+  uint8_t* tiles = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int t = threadIdx.x;
   const int64_t G = cols / M;
   const int buf_bytes = CWB * sub_bytes;
