@@ -157,6 +157,29 @@ __device__ __forceinline__ void tc_st_32x32b_x1(uint32_t taddr, uint32_t a) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 16 consecutive 32-bit columns of the warp's 32 lanes <- / -> 16 registers per thread.
+__device__ __forceinline__ void tc_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld_32x32b_x16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
 
 // ---------------------------------------------------------------- sparse GEMM (CTA pair)
 // A cluster of 2 CTAs computes each 256 x BN output tile with pair MMAs
@@ -279,7 +302,7 @@ enum SpmmEpi : int {
 constexpr int kGatherThreads = P24_GATHER_THREADS;
 static_assert(kGatherThreads % 64 == 0 && kGatherThreads <= 512, "gather threads");
 
-template <int BN, int STAGES, bool kTransOut, int kEpi, bool kGather = false>
+template <int BN, int STAGES, bool kTransOut, int kEpi, bool kGather = false, bool kDrainOk = true>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGatherThreads : 320, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmL,
@@ -291,6 +314,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
   constexpr int kAccBufs = BN > 192 ? 1 : 2;
   static_assert(BN <= 256 && BN % 16 == 0, "tile width");
   static_assert(kAccBufs == 1 ? 256 + 8 * 4 * STAGES <= 512 : 4 * STAGES <= 2 * ((256 - BN) / 8), "TMEM budget");
+  // One accumulator, transposed output: the epilogue drains the tile into bf16 pairs in
+  // the columns after the metadata slots, releases the accumulator, then stores from
+  // there (unless kDrainOk is false; see the epilogue).
+  constexpr bool kDrain = kTransOut && kAccBufs == 1 && kDrainOk;
+  constexpr uint32_t kPackCol = 256 + 8 * 4 * STAGES;
+  static_assert(!kDrain || kPackCol + BN / 2 <= 512, "TMEM budget of the drained tile");
   // gathered B is staged MN-major: [K rows][N columns] in 64-column, 128B-swizzled atoms
   constexpr uint32_t kIdesc = idesc_bf16(2 * kBM, BN, /*sparse=*/true, false, /*b_mn=*/kGather);
   static_assert(!kGather || (!kTransOut && BN == 256), "gathered B: straight output, N = 256 tiles");
@@ -657,56 +686,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
       const uint32_t acc = tmem + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       const int a_row = ta * kBM + q * 32 + lane;  // row of A held by this thread
       if (kTransOut) {
-        // out[j, a_row]: token j (B row) x feature a_row (A row)
+        // out[j, a_row]: token j (B row) x feature a_row (A row). Each chunk of 32 tokens
+        // goes through shared memory as bf16 pairs: row i holds tokens 2i and 2i + 1 of
+        // the chunk, word f the pair of feature f, at word f ^ 4 (i & 7) (conflict-free
+        // both ways). The store phase gives lane l the features n_piece .. n_piece + 7 of
+        // token pairs i = 8r + l / 4.
         const float bias_v = (p.bias && a_row < p.rowsA) ? p.bias[a_row] : 0.f;
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tc_ld_32x32b_x32_wait(acc + c * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float f = __uint_as_float(v[j]) + bias_v;
-            if (p.relu) f = fmaxf(f, 0.f);
-            __nv_bfloat16 hv = __float2bfloat16_rn(f);
-            stage[j * 32 + lane] = *reinterpret_cast<uint16_t*>(&hv);
+        auto act_pair = [&](uint32_t a0, uint32_t a1) {
+          float f0 = __uint_as_float(a0) + bias_v, f1 = __uint_as_float(a1) + bias_v;
+          if (p.relu) {
+            f0 = fmaxf(f0, 0.f);
+            f1 = fmaxf(f1, 0.f);
           }
+          return pack_bf16x2(f0, f1);
+        };
+        const uint32_t pk = tmem + kPackCol + (static_cast<uint32_t>(q * 32) << 16);
+        if (kDrain) {
+          // drain: bias, ReLU and rounding here, then the accumulator is free for the
+          // next tile's MMAs while the stores below run
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32], w[16];
+            tc_ld_32x32b_x32_wait(acc + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = act_pair(v[2 * i], v[2 * i + 1]);
+            tc_st_32x32b_x16(pk + c * 16, w);
+          }
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
+        }
+        uint32_t* stage32 = reinterpret_cast<uint32_t*>(stage);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t w[16];
+          if (kDrain) {
+            tc_ld_32x32b_x16_wait(pk + c * 16, w);
+          } else {
+            uint32_t v[32];
+            tc_ld_32x32b_x32_wait(acc + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = act_pair(v[2 * i], v[2 * i + 1]);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) stage32[i * 32 + (lane ^ ((i & 7) << 2))] = w[i];
           __syncwarp();
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int j = r * 8 + (lane >> 2);
-            const int m = tb * BN + c * 32 + j;
-            const int n = n_piece;
-            uint4 x = *reinterpret_cast<const uint4*>(stage + j * 32 + (lane & 3) * 8);
-            const bool valid = m < p.rowsB && n < p.rowsA;
-            if (valid && kEpi != kEpiFull) {
-              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
-            } else if (valid) {
-              if (p.gate) {
-                const uint32_t gb = (gstage[c * 32 + j] >> (8 * (lane & 3))) & 0xFFu;
-                x.x &= pair_mask(gb, 0);
-                x.y &= pair_mask(gb, 1);
-                x.z &= pair_mask(gb, 2);
-                x.w &= pair_mask(gb, 3);
-              }
-              if (p.a24_vals) {
-                const uint32_t n0 = pick2_nibble(x.x, x.y);
-                const uint32_t n1 = pick2_nibble(x.z, x.w);
-                const uint32_t k0 = kept_pair(x.x, x.y, n0);
-                const uint32_t k1 = kept_pair(x.z, x.w, n1);
-                mask_group(x.x, x.y, n0);
-                mask_group(x.z, x.w, n1);
-                *reinterpret_cast<uint2*>(p.a24_vals + static_cast<int64_t>(m) * p.a24_ldv + n / 2) =
-                    make_uint2(k0, k1);
-                p.a24_meta[static_cast<int64_t>(m) * p.a24_ldm + n / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
-              }
-              if (p.dbias) {
-                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+          for (int r = 0; r < 2; ++r) {
+            const int i = r * 8 + (lane >> 2);
+            const int sw = (i & 7) << 2;
+            const uint4 a = *reinterpret_cast<const uint4*>(stage32 + i * 32 + (((lane & 3) * 8) ^ sw));
+            const uint4 e = *reinterpret_cast<const uint4*>(stage32 + i * 32 + (((lane & 3) * 8 + 4) ^ sw));
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  dsum[2 * i] += __uint_as_float(xw[i] << 16);
-                  dsum[2 * i + 1] += __uint_as_float(xw[i] & 0xFFFF0000u);
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t sel = h ? 0x7632u : 0x5410u;  // token 2i + h: high or low halves
+              uint4 x = make_uint4(__byte_perm(a.x, a.y, sel), __byte_perm(a.z, a.w, sel),
+                                   __byte_perm(e.x, e.y, sel), __byte_perm(e.z, e.w, sel));
+              const int j = 2 * i + h;
+              const int m = tb * BN + c * 32 + j;
+              const int n = n_piece;
+              const bool valid = m < p.rowsB && n < p.rowsA;
+              if (valid && kEpi != kEpiFull) {
+                *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
+              } else if (valid) {
+                if (p.gate) {
+                  const uint32_t gb = (gstage[c * 32 + j] >> (8 * (lane & 3))) & 0xFFu;
+                  x.x &= pair_mask(gb, 0);
+                  x.y &= pair_mask(gb, 1);
+                  x.z &= pair_mask(gb, 2);
+                  x.w &= pair_mask(gb, 3);
                 }
+                if (p.a24_vals) {
+                  const uint32_t n0 = pick2_nibble(x.x, x.y);
+                  const uint32_t n1 = pick2_nibble(x.z, x.w);
+                  const uint32_t k0 = kept_pair(x.x, x.y, n0);
+                  const uint32_t k1 = kept_pair(x.z, x.w, n1);
+                  mask_group(x.x, x.y, n0);
+                  mask_group(x.z, x.w, n1);
+                  *reinterpret_cast<uint2*>(p.a24_vals + static_cast<int64_t>(m) * p.a24_ldv + n / 2) =
+                      make_uint2(k0, k1);
+                  p.a24_meta[static_cast<int64_t>(m) * p.a24_ldm + n / 8] = static_cast<uint8_t>(n0 | (n1 << 4));
+                }
+                if (p.dbias) {
+                  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    dsum[2 * k] += __uint_as_float(xw[k] << 16);
+                    dsum[2 * k + 1] += __uint_as_float(xw[k] & 0xFFFF0000u);
+                  }
+                }
+                *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
               }
-              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) = x;
             }
           }
           __syncwarp();
@@ -741,9 +810,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
+      if (!kDrain) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_cluster(leader_addr(&acc_empty[b]));
+      }
       if (kTransOut && kEpi == kEpiFull && p.dbias) {
         // lanes l, l ^ 4, ..., l ^ 28 hold the same 8 features: sum them, then one
         // fp32 atomic per feature and tile
@@ -1157,17 +1228,25 @@ int num_sms() {
 // bits while the tile's main loop runs, before the accumulator is ready.
 constexpr int kSpBNWide = 256;
 constexpr int kSpBNOverlap = 192;
+// The drained epilogue (one accumulator): the tile is copied out of the accumulator
+// as bf16 pairs and released before its stores, which then overlap the next tile's main
+// loop (70B step: up forward -5%, gated dH -8%; 7B gated dH -14%). A gated tile's gate
+// words are read after those stores, so at short K the next main loop ends first and
+// the drain loses (1.3B dH, K = 2048: +9%); gated tiles drain from this many K-blocks.
+#ifndef P24_DRAIN_GATE_MIN_NKB
+#define P24_DRAIN_GATE_MIN_NKB 32
+#endif
 #ifndef P24_OVERLAP_MAX_NKB
 #define P24_OVERLAP_MAX_NKB 24  // K-blocks (of 128) up to which plain epilogues take the overlapped tile
 #endif
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 6;
 
-template <int BN, bool kTrans, int kEpi, bool kGather = false>
+template <int BN, bool kTrans, int kEpi, bool kGather = false, bool kDrainOk = true>
 cudaError_t run_spmm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& e, const CUtensorMap& l,
                      const CUtensorMap& t, const SpmmParams& p, cudaStream_t s) {
   using L = SpmmSmem<BN, kSpStages>;
-  auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi, kGather>;
+  auto kern = spmm_kernel<BN, kSpStages, kTrans, kEpi, kGather, kDrainOk>;
   const int smem = L::kBytes + 1024;
   constexpr int kThreads = kGather ? 320 + kGatherThreads : 320;  // + the gather warps
   static LaunchSetup setup;
@@ -1259,9 +1338,12 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
     if (heavy_epilogue) return cudaErrorInvalidValue;  // the activation prune is transposed-only
     return run_spmm<kSpBNWide, false, kEpiStore>(ta, tb, te, tl, tt, p, s);
   }
-  if (heavy_epilogue || epi.gate || epi.dbias)
-    return overlap ? run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, tl, tt, p, s)
-                   : run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
+  if (heavy_epilogue || epi.gate || epi.dbias) {
+    if (overlap) return run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
+    return (!epi.gate || p.nkb >= P24_DRAIN_GATE_MIN_NKB)
+               ? run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, tl, tt, p, s)
+               : run_spmm<kSpBNWide, true, kEpiFull, false, false>(ta, tb, te, tl, tt, p, s);
+  }
   return overlap ? run_spmm<kSpBNOverlap, true, kEpiStore>(ta, tb, te, tl, tt, p, s)
                  : run_spmm<kSpBNWide, true, kEpiStore>(ta, tb, te, tl, tt, p, s);
 }
