@@ -114,9 +114,25 @@ __device__ __forceinline__ uint32_t bf16_pos_mask(uint32_t w) {
   return lo | hi;
 }
 
-// One byte of gate bits -> masks for the four bf16 pairs of a 16-byte piece.
-__device__ __forceinline__ uint32_t pair_mask(uint32_t byte, int i) {
-  return (((byte >> (2 * i)) & 1u) ? 0x0000FFFFu : 0u) | (((byte >> (2 * i + 1)) & 1u) ? 0xFFFF0000u : 0u);
+// Byte permute with the sign-replicate selector bit (bit 3 of a selector nibble makes
+// the result byte the selected byte's top bit, repeated).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// One byte of gate bits (bit i: value i of a 16-byte piece of 8 bf16) applied to the
+// piece. Multiplying a nibble by 2^7 + 2^14 + 2^21 + 2^28 moves its bit k to bit 8k + 7
+// (the other partial products land elsewhere and never carry), so each bit becomes a
+// byte's top bit; a sign-replicating permute widens two of those bytes into the 16-bit
+// masks of one word.
+__device__ __forceinline__ void apply_gate(uint4& x, uint32_t byte) {
+  const uint32_t s0 = ((byte & 0xFu) * 0x10204080u) & 0x80808080u;
+  const uint32_t s1 = ((byte >> 4) * 0x10204080u) & 0x80808080u;
+  x.x &= prmt(s0, 0u, 0x9988u);
+  x.y &= prmt(s0, 0u, 0xBBAAu);
+  x.z &= prmt(s1, 0u, 0x9988u);
+  x.w &= prmt(s1, 0u, 0xBBAAu);
 }
 // Bit i set where bf16 value i of the piece is > 0.
 __device__ __forceinline__ uint32_t positive_bits(const uint4& x) {
@@ -218,7 +234,7 @@ struct SpmmSmem {
 template <int BN>
 __device__ __forceinline__ uint32_t meta_col(int s, int j) {
   const int k = 4 * s + j;
-  if constexpr (BN > 192) return 256 + 8 * k;  // one accumulator buffer: slots fill [256, 512)
+  if constexpr (BN > 192) return 256 + 8 * k;  // one accumulator buffer: slots fill [256, 256 + 32 STAGES)
   constexpr int kGap = (256 - BN) / 8;  // slots per gap
   return k < kGap ? BN + 8 * k : 256 + BN + 8 * (k - kGap);
 }
@@ -750,10 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
               } else if (valid) {
                 if (p.gate) {
                   const uint32_t gb = (gstage[c * 32 + j] >> (8 * (lane & 3))) & 0xFFu;
-                  x.x &= pair_mask(gb, 0);
-                  x.y &= pair_mask(gb, 1);
-                  x.z &= pair_mask(gb, 2);
-                  x.w &= pair_mask(gb, 3);
+                  apply_gate(x, gb);
                 }
                 if (p.a24_vals) {
                   const uint32_t n0 = pick2_nibble(x.x, x.y);
@@ -1222,10 +1235,10 @@ int num_sms() {
 }
 
 // Sparse tile widths: N = 256 (one TMEM accumulator, the most MMA work buffered
-// per shared-memory byte) unless the epilogue prunes activations; that one takes
-// N = 192 with two accumulators, so that its longer epilogue overlaps the next
-// tile's main loop. The ReLU' gate stays on N = 256: the epilogue turns it into
-// bits while the tile's main loop runs, before the accumulator is ready.
+// per shared-memory byte, the epilogue overlapped through the drained copy below),
+// except for plain epilogues with very short main loops, which take N = 192 with two
+// accumulators. The ReLU' gate turns into bits while the tile's main loop runs,
+// before the accumulator is ready.
 constexpr int kSpBNWide = 256;
 constexpr int kSpBNOverlap = 192;
 // The drained epilogue (one accumulator): the tile is copied out of the accumulator
@@ -1237,7 +1250,7 @@ constexpr int kSpBNOverlap = 192;
 #define P24_DRAIN_GATE_MIN_NKB 32
 #endif
 #ifndef P24_OVERLAP_MAX_NKB
-#define P24_OVERLAP_MAX_NKB 24  // K-blocks (of 128) up to which plain epilogues take the overlapped tile
+#define P24_OVERLAP_MAX_NKB 8  // K-blocks (of 128) up to which plain epilogues take the two-accumulator tile
 #endif
 constexpr int kSpStages = 4;
 constexpr int kDwStages = 6;
@@ -1274,12 +1287,12 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
                         bool transposed_out, const EpiArgs& epi, int* status, cudaStream_t s) {
   if (A.rows == 0 || rowsB == 0) return cudaSuccess;
   const bool heavy_epilogue = epi.act24.vals != nullptr;
-  // Two accumulators (the epilogue of a tile overlaps the next tile's main loop) at the
-  // narrower tile when the epilogue is heavy, or when the main loop is short and the
-  // epilogue plain (measured: the short-K up forward of GPT-2 and 1.3B gains 4-12%; the
-  // gated dH does not).
-  const bool overlap = transposed_out && (heavy_epilogue || (!epi.gate && !epi.dbias &&
-                                                             (A.cols + 127) / 128 <= P24_OVERLAP_MAX_NKB));
+  // Two accumulators at the narrower tile only for plain epilogues of very short main
+  // loops (GPT-2, K = 768). Measured against N = 256 with the drained epilogue: the 1.3B
+  // up forward (K = 2048) is 12% faster on N = 256, the 7B up forward with the 2:4
+  // activation prune 17% faster, GPT-2 1% slower.
+  const bool overlap = transposed_out && !heavy_epilogue && !epi.gate && !epi.dbias &&
+                       (A.cols + 127) / 128 <= P24_OVERLAP_MAX_NKB;
   const int BN = overlap ? kSpBNOverlap : kSpBNWide;
   SpmmParams p{};
   p.rowsA = static_cast<int>(A.rows);
@@ -1339,7 +1352,6 @@ cudaError_t launch_spmm(const p24_sparse& A, const void* B, int64_t rowsB, int64
     return run_spmm<kSpBNWide, false, kEpiStore>(ta, tb, te, tl, tt, p, s);
   }
   if (heavy_epilogue || epi.gate || epi.dbias) {
-    if (overlap) return run_spmm<kSpBNOverlap, true, kEpiFull>(ta, tb, te, tl, tt, p, s);
     return (!epi.gate || p.nkb >= P24_DRAIN_GATE_MIN_NKB)
                ? run_spmm<kSpBNWide, true, kEpiFull>(ta, tb, te, tl, tt, p, s)
                : run_spmm<kSpBNWide, true, kEpiFull, false, false>(ta, tb, te, tl, tt, p, s);
