@@ -107,11 +107,11 @@ __device__ __forceinline__ void tile_coords(int t, int tilesA, int tilesB, int g
   tb = r / gsize;
 }
 
-__device__ __forceinline__ uint32_t bf16_pos_mask(uint32_t w) {
-  // per 16-bit half: 0xFFFF where the bf16 value is > 0 (sign clear, not +0)
-  const uint32_t lo = ((w & 0x8000u) == 0 && (w & 0x7FFFu) != 0) ? 0x0000FFFFu : 0u;
-  const uint32_t hi = ((w & 0x80000000u) == 0 && (w & 0x7FFF0000u) != 0) ? 0xFFFF0000u : 0u;
-  return lo | hi;
+// Per 16-bit half: the top bit set where the bf16 value is > 0 (sign clear, magnitude
+// nonzero; the sum of a magnitude and 0x7FFF reaches bit 15 exactly when it is nonzero,
+// and never carries into the other half).
+__device__ __forceinline__ uint32_t bf16_pos_bits(uint32_t w) {
+  return (((w & 0x7FFF7FFFu) + 0x7FFF7FFFu) & ~w) & 0x80008000u;
 }
 
 // Byte permute with the sign-replicate selector bit (bit 3 of a selector nibble makes
@@ -134,16 +134,13 @@ __device__ __forceinline__ void apply_gate(uint4& x, uint32_t byte) {
   x.z &= prmt(s1, 0u, 0x9988u);
   x.w &= prmt(s1, 0u, 0xBBAAu);
 }
-// Bit i set where bf16 value i of the piece is > 0.
+// Bit i set where bf16 value i of the piece is > 0: the 8 flags sit at bits 15 and 31 of
+// the four words; shifts by 15, 13, 11 and 9 put them at bits 0, 2, 4, 6 and 16, 18, 20,
+// 22, and folding the upper half down by 15 interleaves them.
 __device__ __forceinline__ uint32_t positive_bits(const uint4& x) {
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-  uint32_t b = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t m = bf16_pos_mask(w[i]);
-    b |= ((m & 1u) << (2 * i)) | (((m >> 16) & 1u) << (2 * i + 1));
-  }
-  return b;
+  const uint32_t s = (bf16_pos_bits(x.x) >> 15) | (bf16_pos_bits(x.y) >> 13) | (bf16_pos_bits(x.z) >> 11) |
+                     (bf16_pos_bits(x.w) >> 9);
+  return (s | (s >> 15)) & 0xFFu;
 }
 
 // 2:4 pick on a group held as two words (see prune24_kernels.cu for the key).
@@ -668,28 +665,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
       if (kTransOut && kEpi == kEpiFull && p.gate) {
         // The ReLU' gate of this warp's 32 features, one word per token (bit l:
         // gate(m, n_warp + l) > 0), read from the bf16 gate while the tile's main
-        // loop still runs, so that no load sits in the epilogue's critical path.
-        // Four tokens per lane at a time: their 16 loads are all issued before any is used.
-        for (int j0 = lane; j0 < BN; j0 += 128) {
-          uint4 x[4][4];
+        // loop still runs, so that no load sits in the epilogue's critical path. Lanes
+        // 4i .. 4i + 3 read the 64 contiguous bytes of one token's 32 features, 16 bytes
+        // each, so a load instruction covers 8 tokens in whole sectors; 16 loads per lane
+        // are issued before any is used, and each lane writes its byte of the word.
+        uint8_t* gbytes = reinterpret_cast<uint8_t*>(gstage);
+        const int kp = lane & 3;
+        const bool col_in = n_warp + 8 * kp < p.rowsA;
+        const uint16_t* gcol = p.gate + n_warp + 8 * kp;
+        for (int j0 = lane >> 2; j0 < BN; j0 += 128) {
+          uint4 x[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = j0 + 32 * u;
+          for (int u = 0; u < 16; ++u) {
+            const int j = j0 + 8 * u;
             const int m = tb * BN + j;
-            const bool row_in = j < BN && m < p.rowsB;
-            const uint16_t* g = p.gate + static_cast<int64_t>(m) * p.ldg + n_warp;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              x[u][k] = row_in && n_warp + 8 * k < p.rowsA ? __ldg(reinterpret_cast<const uint4*>(g + 8 * k))
-                                                          : make_uint4(0, 0, 0, 0);
+            x[u] = (j < BN && m < p.rowsB && col_in)
+                       ? __ldg(reinterpret_cast<const uint4*>(gcol + static_cast<int64_t>(m) * p.ldg))
+                       : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = j0 + 32 * u;
-            uint32_t word = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) word |= positive_bits(x[u][k]) << (8 * k);
-            if (j < BN) gstage[j] = word;
+          for (int u = 0; u < 16; ++u) {
+            const int j = j0 + 8 * u;
+            if (j < BN) gbytes[4 * j + kp] = static_cast<uint8_t>(positive_bits(x[u]));
           }
         }
         __syncwarp();
