@@ -658,8 +658,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? 320 + kGat
       ta = 2 * ta + rank;
       const int b = kAccBufs == 2 ? (tl & 1) : 0;
       const uint32_t aph = kAccBufs == 2 ? ((tl >> 1) & 1) : (tl & 1);
-      // Transposed output: in the store phase lane l handles token j = 8r + l / 4 of
-      // each chunk and features n_piece .. n_piece + 7 of the tile.
+      // Transposed output: in the store phase lane l handles tokens 2i, 2i + 1 (i = 8r +
+      // l / 4) of each chunk and features n_piece .. n_piece + 7 of the tile.
       const int n_warp = ta * kBM + q * 32;
       const int n_piece = n_warp + (lane & 3) * 8;
       if (kTransOut && kEpi == kEpiFull && p.gate) {
